@@ -1,0 +1,454 @@
+"""Benchmark of the blockwise-FP8 linear layer on B300: fwd + dgrad + wgrad at Puro-2B shapes.
+
+One step = the whole hot path for every linear of the workload: quantise x
+(1x128), quantise W (128x128), forward GEMM; quantise dy, input-gradient GEMM;
+quantise dy and x transposed, weight-gradient GEMM (8 kernels per linear).
+The metric is TFLOPS of the three GEMMs (3 x 2MNK per linear) over the whole
+step time, quantisers included.
+
+Default workload: the Puro-2B MLP at M = 8192 tokens (gate/up 2048 -> 12288,
+down 6144 -> 2048, Student-t(3) activations), the shapes the FP8-peak target is
+quoted on. Inputs are synthetic and seeded (workloads.py); every step's inputs
+(about 0.4 GB) exceed the 126 MB L2, so no flush is needed between steps.
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload mlp|attn|stack|single]
+For N > 1 launch one process per GPU with torch.distributed.run; the path has
+no exchange step ("replicas only"), every rank runs its own replica and the
+result is the sum of the ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "blockwise-FP8 linear TFLOPS (fwd+dgrad+wgrad) at Puro-2B shapes, % of FP8 peak"
+UNIT = "TFLOPS"
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio on B300 (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["mlp", "attn", "stack", "single"], default="mlp")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workload(name: str) -> wl.Workload:
+    return {"mlp": wl.mlp_projections, "attn": wl.attention_projections,
+            "stack": wl.full_stack, "single": wl.single_linear_256}[name]()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int, backend: str):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return rank, local, ws
+
+
+def allreduce_max(v: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.2)
+
+    def result(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: the upper part of the power trace
+        load = [s for s, p in zip(sm, pw) if p >= 0.5 * max(pw)] or sm
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": float(max(pw))}
+
+
+# ---------------------------------------------------------------------------- CPU oracle sample
+class OracleSample:
+    """The oracle (as it stands) on a bounded sample of the workload, on the host cores.
+
+    prepare(): synthetic inputs and their oracle codes (not timed).
+    run(r): for every linear, the quantisers on r-row slices of x, dy and W (x also
+    transposed), the forward and input-gradient GEMMs on r output rows and the
+    weight-gradient GEMM on r rows of dW (contracting over all M tokens).
+    Returns (seconds, GEMM flops of the sample).
+    """
+
+    def __init__(self, work: wl.Workload):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.work = work
+        self.data = []
+        for lin in work.linears:
+            x, w, dy = wl.make_linear(lin)
+            qx, sx = oracle.quantize_act(x)
+            qw, sw = oracle.quantize_weight(w)
+            qdy, sdy = oracle.quantize_act(dy)
+            qdyt, sdyt = oracle.quantize_transpose(dy)
+            qxt, sxt = oracle.quantize_transpose(x)
+            self.data.append((lin, x, w, dy, (qx, sx, qw, sw, qdy, sdy, qdyt, sdyt, qxt, sxt)))
+
+    def run(self, r: int):
+        o = self.oracle
+        flops = 0
+        t0 = time.perf_counter()
+        for lin, x, w, dy, (qx, sx, qw, sw, qdy, sdy, qdyt, sdyt, qxt, sxt) in self.data:
+            rm = np.arange(min(r, lin.M))
+            rn = np.arange(min(r, lin.N))
+            o.quantize_act(x[:rm.size])
+            o.quantize_weight(w[:(rn.size + 127) // 128 * 128])
+            o.gemm_fwd(qx, sx, qw, sw, rows=rm)
+            flops += 2 * rm.size * lin.N * lin.K
+            if "dgrad" in self.work.passes:
+                o.quantize_act(dy[:rm.size])
+                o.gemm_dgrad(qdy, sdy, qw, sw, rows=rm)
+                flops += 2 * rm.size * lin.N * lin.K
+            if "wgrad" in self.work.passes:
+                o.quantize_transpose(dy[:rm.size])
+                o.quantize_transpose(x[:rm.size])
+                o.gemm_wgrad(qdyt, sdyt, qxt, sxt, lin.M, rows=rn)
+                flops += 2 * rn.size * lin.M * lin.K
+        return time.perf_counter() - t0, flops
+
+    def calibrate(self, target_s: float):
+        """Smallest power-of-two-ish row count whose run takes about target_s seconds."""
+        r = 2
+        dt, fl = self.run(r)
+        while dt < target_s / 2 and r < 1 << 14:
+            r = int(min(r * max(2.0, 0.8 * target_s / max(dt, 1e-3)), 1 << 14))
+            dt, fl = self.run(r)
+        return r, dt, fl
+
+    @staticmethod
+    def cores():
+        try:
+            return len(os.sched_getaffinity(0))
+        except AttributeError:
+            return os.cpu_count()
+
+    def describe(self, r: int, dt: float) -> str:
+        return (f"oracle (FP64, OpenMP) on {r} output rows per GEMM pass of every linear of {self.work.name} "
+                f"plus the quantisers on {r}-row slices; {dt:.2f} s per sample")
+
+
+def cpu_oracle_sample(work: wl.Workload, target_s: float):
+    s = OracleSample(work)
+    r, dt, fl = s.calibrate(target_s)
+    return fl / dt / 1e12, s.cores(), {"sample": s.describe(r, dt)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    rank, local, ws = dist_setup(args.gpus, "nccl")
+    torch.cuda.set_device(local)
+    import blockwise_fp8_linear_weight_b300 as bfp8
+    from blockwise_fp8_linear_weight_b300 import build as lib_build
+    lib_build.build()
+    bfp8.load_library()
+
+    work = workload(args.workload)
+    dev = torch.device("cuda", local)
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    layers, inputs, host = [], [], []
+    for lin in work.linears:
+        x, w, dy = wl.make_linear(lin)
+        layers.append(bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev))
+        inputs.append((up(x), up(w), up(dy)))
+        if not args.no_e2e:
+            host.append(tuple(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+                              for a in (x, w, dy)))
+    fwd_only = work.passes == ("fwd",)
+
+    def step():
+        for L, (x, w, dy) in zip(layers, inputs):
+            L.forward(x, w)
+            if not fwd_only:
+                L.backward(dy)
+
+    kernels_per_step = sum(3 if fwd_only else 8 for _ in layers)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert bfp8.last_device_status() == 0, "a kernel timed out during warm-up"
+
+    # ------------------------------------------------------------ timed region
+    # per-GEMM events around every GEMM launch of the timed steps (same stream)
+    gemm_events = {"fwd": [], "dgrad": [], "wgrad": []}
+    gemm_flops = {"fwd": 0, "dgrad": 0, "wgrad": 0}
+
+    def timed_step():
+        for L, (x, w, dy), lin in zip(layers, inputs, work.linears):
+            bfp8.fp8_quantize_act(x, L.qx, L.sx)
+            bfp8.fp8_quantize_weight(w, L.qw, L.sw)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+            e1.record(stream)
+            gemm_events["fwd"].append((e0, e1, 2 * lin.M * lin.N * lin.K))
+            if fwd_only:
+                continue
+            bfp8.fp8_quantize_act(dy, L.qdy, L.sdy)
+            e2 = torch.cuda.Event(enable_timing=True)
+            e3 = torch.cuda.Event(enable_timing=True)
+            e2.record(stream)
+            bfp8.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
+            e3.record(stream)
+            gemm_events["dgrad"].append((e2, e3, 2 * lin.M * lin.N * lin.K))
+            bfp8.fp8_quantize_transpose(dy, L.qdyt, L.sdyt)
+            bfp8.fp8_quantize_transpose(x, L.qxt, L.sxt)
+            e4 = torch.cuda.Event(enable_timing=True)
+            e5 = torch.cuda.Event(enable_timing=True)
+            e4.record(stream)
+            bfp8.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, lin.M, L.dw)
+            e5.record(stream)
+            gemm_events["wgrad"].append((e4, e5, 2 * lin.M * lin.N * lin.K))
+
+    with ClockSampler(local) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            timed_step()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    clocks = clk.result()
+    status = bfp8.last_device_status()
+    ms_local = t_start.elapsed_time(t_end)
+    ms = allreduce_max(ms_local, ws, dev)
+    total_flops = work.flops * args.steps * ws
+    tflops = total_flops / (ms / 1e3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    fp8_peak_sustained = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    per_kernel = {}
+    for k, evs in gemm_events.items():
+        if not evs:
+            continue
+        t = sum(a.elapsed_time(b) for a, b, _ in evs)
+        fl = sum(f for _, _, f in evs)
+        per_kernel[k] = {"launches": len(evs), "ms_total": round(t, 3), "avg_us": round(1e3 * t / len(evs), 2),
+                         "tflops": round(fl / (t / 1e3) / 1e12, 1), "share_of_step": round(t / ms_local, 4)}
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
+    achieved = per_kernel[dom]["tflops"]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f)
+        if tr.get("workload") == work.name and tr.get("kernel") == dom and tr.get("source_sha") == _gemm_sha():
+            traffic = tr.get("dram_bytes_per_launch")
+    roofline = {"bound": "tensor", "kernel": f"bfp8_gemm_kernel ({dom})", "achieved": achieved,
+                "peak": round(fp8_peak_sustained, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp8_peak_sustained, 4), "traffic": traffic,
+                "peak_source": (f"{peak_src}: 2 x bf16_tflops_sustained ({peaks['bf16_tflops_sustained']}) "
+                                f"from MEASURED_PEAKS.json, FP8/BF16 nominal ratio 2")}
+
+    # ------------------------------------------------------------ end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        dev_in = [tuple(torch.empty_like(t, device=dev) for t in h) for h in host]
+        outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.y, L.dx, L.dw))
+                     for L in layers]
+        bi = sum(t.numel() * 2 for h in host for t in h)
+        bo = sum(t.numel() * 2 for L in layers for t in ((L.y,) if fwd_only else (L.y, L.dx, L.dw)))
+        e2e_steps = max(3, min(args.steps, 50))
+
+        def e2e_step():
+            for L, h, d, o in zip(layers, host, dev_in, outs_host):
+                for src, dst in zip(h, d):
+                    dst.copy_(src, non_blocking=True)
+                L.forward(d[0], d[1])
+                o[0].copy_(L.y, non_blocking=True)
+                if not fwd_only:
+                    L.backward(d[2])
+                    o[1].copy_(L.dx, non_blocking=True)
+                    o[2].copy_(L.dw, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(ws)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = allreduce_max(s0.elapsed_time(s1), ws, dev)
+        e2e = {"value": round(work.flops * e2e_steps * ws / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+               "how": "pinned host x, W, dy copied in and y, dx, dW copied out every step, same stream"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, cores, info = cpu_oracle_sample(work, args.cpu_seconds)
+        cpu = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": info["sample"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(tflops, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+            "pct_of_fp8_peak": round(100 * tflops / fp8_peak_sustained, 2),
+            "config": {"workload": work.name, "linears": [f"{l.name}: M={l.M} K={l.K} N={l.N} x~{l.x_dist}"
+                                                          for l in work.linears],
+                       "passes": "+".join(work.passes) + " incl. all quantisers",
+                       "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (no flush)"},
+            "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": kernels_per_step * args.steps, "clocks": clocks,
+            "device_status": bfp8.STATUS.get(status, status),
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _gemm_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "blockwise_fp8_linear_weight_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    """The oracle on the host cores, timed as it stands: each step is one bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    work = workload(args.workload)
+    sampler = OracleSample(work)
+    per_step = max(0.2, 90.0 / max(1, args.steps + args.warmup))
+    r, dt, _ = sampler.calibrate(per_step)
+    for _ in range(args.warmup):
+        sampler.run(r)
+    tot_t, tot_f = 0.0, 0
+    for _ in range(args.steps):
+        dt, fl = sampler.run(r)
+        tot_t += dt
+        tot_f += fl
+    v = tot_f / tot_t / 1e12
+    line = {
+        "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": work.name, "passes": "+".join(work.passes),
+                   "parallelism": "host cores (OpenMP)", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": sampler.cores(), "kind": "oracle",
+                         "sample": sampler.describe(r, tot_t / args.steps)},
+        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+"""Blockwise-FP8 linear layer for B300 (sm_103a): Python binding of the C ABI in include/bfp8.h.
+
+The binding only marshals arguments: it takes CUDA tensors (torch is used for
+device memory and streams), allocates outputs when none are given, and calls
+``libbfp8.so`` through ctypes on the current torch stream. Every step of the
+path runs in the library's CUDA kernels; there is no CPU fallback. If the
+library is missing or the device is not a B300, calls raise.
+
+Entry points (same names as the C ABI):
+  fp8_quantize_act(x)            -> (q [R,C] u8, s [C/128, R] f32)
+  fp8_quantize_weight(w)         -> (q [N,K] u8, s [N/128, K/128] f32)
+  fp8_quantize_transpose(x)      -> (qt [C, R128] u8, st [R128/128, C] f32)
+  fp8_block_gemm_fwd(qx, sx, qw, sw)        -> y  [M, N] bf16
+  fp8_block_gemm_dgrad(qdy, sdy, qw, sw)    -> dx [M, K] bf16
+  fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M) -> dw [N, K] bf16
+Scale tensors are allocated with a row stride rounded up to 4 elements so that
+the GEMMs' TMA loads see 16-byte rows; the returned tensors are views of the
+valid columns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+LIB_PATH = os.path.join(_PKG, "libbfp8.so")
+HEADER_PATH = os.path.join(_ROOT, "include", "bfp8.h")
+TILE = 128
+
+STATUS = {0: "BFP8_OK", -1: "BFP8_EINVAL", -2: "BFP8_EALIGN", -3: "BFP8_ESHAPE",
+          -4: "BFP8_ELAUNCH", -5: "BFP8_ETIMEOUT", -6: "BFP8_EARCH"}
+
+
+class Bfp8Error(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libbfp8.so and declare its signatures. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libbfp8.so not found at {path}; build it with "
+                          f"`python -m blockwise_fp8_linear_weight_b300.build`")
+    lib = ctypes.CDLL(path)
+    i64, p, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    sig = {
+        "fp8_quantize_act": [p, i64, i64, i64, p, i64, p, i64, p],
+        "fp8_quantize_weight": [p, i64, i64, i64, p, i64, p, p],
+        "fp8_quantize_transpose": [p, i64, i64, i64, p, i64, p, i64, p],
+        "fp8_block_gemm_fwd": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
+        "fp8_block_gemm_dgrad": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
+        "fp8_block_gemm_wgrad": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
+        "bfp8_last_device_status": [p],
+        "bfp8_set_gemm_tile_n": [c_int],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = c_int
+    lib.bfp8_status_string.argtypes = [c_int]
+    lib.bfp8_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def header_functions(path: str = HEADER_PATH):
+    """Names of the functions declared in include/bfp8.h."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        msg = load_library().bfp8_status_string(rc).decode()
+        raise Bfp8Error(fn, rc, msg)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _req(t, dtype, name, ndim=2):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or (ndim == 2 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be a row-major 2-D tensor with unit column stride")
+    return t
+
+
+def _round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+def _scales(chunks: int, n: int, device):
+    """[chunks, n] float32 view of a buffer whose row stride is n rounded up to 4."""
+    buf = torch.empty((chunks, max(_round_up(n, 4), 4)), dtype=torch.float32, device=device)
+    return buf[:, :n]
+
+
+# ----------------------------------------------------------------------- quantisers
+def fp8_quantize_act(x, q=None, s=None):
+    """1x128 tiles along the columns of x [R, C] (bf16). Returns (q, s)."""
+    lib = load_library()
+    _req(x, torch.bfloat16, "x")
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device) if q is None else q
+    s = _scales(C // TILE if C % TILE == 0 else 0, R, x.device) if s is None else s
+    _check("fp8_quantize_act", lib.fp8_quantize_act(
+        _ptr(x), R, C, x.stride(0), _ptr(q), q.stride(0), _ptr(s), s.stride(0), _stream()))
+    return q, s
+
+
+def fp8_quantize_weight(w, q=None, s=None):
+    """128x128 blocks of w [N, K] (bf16). Returns (q, s) with s [N/128, K/128]."""
+    lib = load_library()
+    _req(w, torch.bfloat16, "w")
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    s = torch.empty((N // TILE, K // TILE), dtype=torch.float32, device=w.device) if s is None else s
+    if s.dim() != 2 or not s.is_contiguous():
+        raise ValueError("weight scales must be a dense [N/128, K/128] tensor")
+    _check("fp8_quantize_weight", lib.fp8_quantize_weight(
+        _ptr(w), N, K, w.stride(0), _ptr(q), q.stride(0), _ptr(s), _stream()))
+    return q, s
+
+
+def fp8_quantize_transpose(x, qt=None, st=None):
+    """Tiles of 128 rows of x [R, C] (bf16), written transposed. Returns (qt [C, R128], st [R128/128, C])."""
+    lib = load_library()
+    _req(x, torch.bfloat16, "x")
+    R, C = x.shape
+    R128 = _round_up(R, TILE)
+    qt = torch.empty((C, R128), dtype=torch.uint8, device=x.device) if qt is None else qt
+    if st is None:
+        st = torch.empty((R128 // TILE, _round_up(C, 4)), dtype=torch.float32, device=x.device)[:, :C]
+    _check("fp8_quantize_transpose", lib.fp8_quantize_transpose(
+        _ptr(x), R, C, x.stride(0), _ptr(qt), qt.stride(0), _ptr(st), st.stride(0), _stream()))
+    return qt, st
+
+
+# ----------------------------------------------------------------------- GEMMs
+def fp8_block_gemm_fwd(qx, sx, qw, sw, y=None):
+    """y [M, N] bf16 = blockwise-FP8 x W^T from (qx [M,K], sx [K/128, M], qw [N,K], sw [N/128, K/128])."""
+    lib = load_library()
+    M, K = qx.shape
+    N = qw.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    _check("fp8_block_gemm_fwd", lib.fp8_block_gemm_fwd(
+        _ptr(qx), qx.stride(0), _ptr(sx), sx.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
+        _ptr(y), y.stride(0), M, N, K, _stream()))
+    return y
+
+
+def fp8_block_gemm_dgrad(qdy, sdy, qw, sw, dx=None):
+    """dx [M, K] bf16 = blockwise-FP8 dy W from (qdy [M,N], sdy [N/128, M], qw [N,K], sw [N/128, K/128])."""
+    lib = load_library()
+    M, N = qdy.shape
+    K = qw.shape[1]
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=qdy.device) if dx is None else dx
+    _check("fp8_block_gemm_dgrad", lib.fp8_block_gemm_dgrad(
+        _ptr(qdy), qdy.stride(0), _ptr(sdy), sdy.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
+        _ptr(dx), dx.stride(0), M, N, K, _stream()))
+    return dx
+
+
+def fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M, dw=None):
+    """dw [N, K] bf16 = blockwise-FP8 dy^T x from transposed tiles (qdyt [N,M128], qxt [K,M128])."""
+    lib = load_library()
+    N = qdyt.shape[0]
+    K = qxt.shape[0]
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device=qdyt.device) if dw is None else dw
+    _check("fp8_block_gemm_wgrad", lib.fp8_block_gemm_wgrad(
+        _ptr(qdyt), qdyt.stride(0), _ptr(sdyt), sdyt.stride(0), _ptr(qxt), qxt.stride(0),
+        _ptr(sxt), sxt.stride(0), _ptr(dw), dw.stride(0), M, N, K, _stream()))
+    return dw
+
+
+def last_device_status() -> int:
+    """Synchronise the current stream and read/clear the kernels' bounded-wait status word."""
+    return load_library().bfp8_last_device_status(_stream())
+
+
+def set_gemm_tile_n(tile_n: int) -> int:
+    """GEMM output tile width: 0 (automatic), 128 or 256. Returns the previous value."""
+    rc = load_library().bfp8_set_gemm_tile_n(int(tile_n))
+    if rc < 0:
+        raise ValueError("tile_n must be 0, 128 or 256")
+    return rc
+
+
+# ----------------------------------------------------------------------- one linear layer
+class BlockwiseFP8Linear:
+    """Buffers and call sequence of one blockwise-FP8 linear layer y = x W^T (x [M,K], W [N,K]).
+
+    ``forward(x, w)`` quantises x (1x128) and W (128x128) and runs the forward
+    GEMM; ``backward(dy)`` quantises dy (1x128 along N, and transposed along M),
+    quantises x transposed, and runs the input- and weight-gradient GEMMs. All
+    outputs live in buffers allocated once, so a training step launches exactly
+    eight kernels and allocates nothing.
+    """
+
+    def __init__(self, M: int, K: int, N: int, device="cuda"):
+        self.M, self.K, self.N = M, K, N
+        dev = torch.device(device)
+        M128 = _round_up(M, TILE)
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        self.qx = torch.empty((M, K), dtype=u8, device=dev)
+        self.sx = _scales(K // TILE, M, dev)
+        self.qw = torch.empty((N, K), dtype=u8, device=dev)
+        self.sw = torch.empty((N // TILE, K // TILE), dtype=f32, device=dev)
+        self.qdy = torch.empty((M, N), dtype=u8, device=dev)
+        self.sdy = _scales(N // TILE, M, dev)
+        self.qdyt = torch.empty((N, M128), dtype=u8, device=dev)
+        self.sdyt = _scales(M128 // TILE, N, dev)
+        self.qxt = torch.empty((K, M128), dtype=u8, device=dev)
+        self.sxt = _scales(M128 // TILE, K, dev)
+        self.y = torch.empty((M, N), dtype=bf, device=dev)
+        self.dx = torch.empty((M, K), dtype=bf, device=dev)
+        self.dw = torch.empty((N, K), dtype=bf, device=dev)
+        self._x = None
+
+    def forward(self, x, w):
+        fp8_quantize_act(x, self.qx, self.sx)
+        fp8_quantize_weight(w, self.qw, self.sw)
+        fp8_block_gemm_fwd(self.qx, self.sx, self.qw, self.sw, self.y)
+        self._x = x
+        return self.y
+
+    def backward(self, dy):
+        fp8_quantize_act(dy, self.qdy, self.sdy)
+        fp8_block_gemm_dgrad(self.qdy, self.sdy, self.qw, self.sw, self.dx)
+        fp8_quantize_transpose(dy, self.qdyt, self.sdyt)
+        fp8_quantize_transpose(self._x, self.qxt, self.sxt)
+        fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw)
+        return self.dx, self.dw
+
+    KERNELS_PER_STEP = 8

@@ -1,0 +1,424 @@
+// C ABI of the blockwise-FP8 linear-layer library (declared in include/bfp8.h):
+// host-side argument checks, TMA tensor-map encoding and kernel launches.
+// Everything the path computes runs in the kernels of quant.cuh and gemm.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "bfp8.h"
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace bfp8 {
+
+// Set (OR-ed) by a kernel that gives up on a bounded wait.
+__device__ unsigned g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;  // TMA coordinates are int32
+constexpr int64_t kMaxGridY = 65535;
+
+std::atomic<int> g_tile_n{0};
+
+// ----------------------------------------------------------------- helpers
+bool aligned(const void* p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Compute capability 10.3 check, cached per device.
+int check_arch(int* dev_out)
+{
+    static std::atomic<int> cache[kMaxDevices];  // 0 unknown, 1 ok, 2 wrong arch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return BFP8_ELAUNCH;
+    if (dev_out)
+        *dev_out = dev;
+    int c = cache[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        c = (major == 10 && minor == 3) ? 1 : 2;
+        cache[dev].store(c, std::memory_order_relaxed);
+    }
+    return c == 1 ? BFP8_OK : BFP8_EARCH;
+}
+
+unsigned* device_status_ptr(int dev)
+{
+    static std::atomic<unsigned*> cache[kMaxDevices];
+    unsigned* p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_device_status) != cudaSuccess)
+            return nullptr;
+        p = static_cast<unsigned*>(q);
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D tensor map over a row-major [outer][inner] array with the given row stride.
+bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? BFP8_OK : BFP8_ELAUNCH;
+}
+
+// ----------------------------------------------------------------- GEMM launch
+struct GemmProblem {
+    // A: codes [gm][ld_a] with the contraction axis (gk) contiguous
+    const uint8_t* a;
+    int64_t lda;
+    // B: codes; K-major [gn][ld_b] (contraction contiguous) or MN-major [gk][ld_b]
+    const uint8_t* b;
+    int64_t ldb;
+    bool b_mn;
+    // A scales [gk/128][ld_sa]
+    const float* sa;
+    int64_t ld_sa;
+    // B scales: vector [gk/128][ld_sb], or scalar table with strides
+    const float* sb;
+    int64_t ld_sb;
+    bool sb_vec;
+    int64_t sb_col_stride, sb_chunk_stride;
+    void* d;
+    int64_t ldd;
+    int64_t gm, gn, gk;
+};
+
+template <class Cfg>
+int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int dev)
+{
+    CUtensorMap tmA, tmB, tmSA, tmSB, tmD;
+    const int64_t nc = p.gk / 128;
+    bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, p.gk, p.gm, p.lda, 128, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (Cfg::B_MN)
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gn, p.gk, p.ldb, 128, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, 1,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (Cfg::SB_VEC)
+        ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sb, p.gn, nc, p.ld_sb * 4, Cfg::BN, 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+        tmSB = tmSA;  // unused in scalar mode
+    ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.d, p.gn, p.gm, p.ldd * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok)
+        return BFP8_ELAUNCH;
+
+    static std::atomic<bool> attr_set[kMaxDevices];
+    auto kern = bfp8_gemm_kernel<Cfg>;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+            cudaSuccess)
+            return BFP8_ELAUNCH;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    GemmArgs args;
+    args.gm = static_cast<int>(p.gm);
+    args.gn = static_cast<int>(p.gn);
+    args.num_chunks = static_cast<int>(nc);
+    args.sb_scalar = p.sb;
+    args.sb_col_stride = p.sb_col_stride;
+    args.sb_chunk_stride = p.sb_chunk_stride;
+    args.status = status;
+    dim3 grid(static_cast<unsigned>((p.gn + Cfg::BN - 1) / Cfg::BN), static_cast<unsigned>((p.gm + 127) / 128));
+    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
+    return launch_status();
+}
+
+template <bool B_MN, bool SB_VEC>
+int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
+{
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    unsigned* status = device_status_ptr(dev);
+    if (!status)
+        return BFP8_ELAUNCH;
+    int tn = g_tile_n.load(std::memory_order_relaxed);
+    if (tn == 0)
+        tn = 128;
+    if (tn == 256)
+        return run_gemm<GemmConfig<256, 4, B_MN, SB_VEC>>(p, status, stream, dev);
+    return run_gemm<GemmConfig<128, 6, B_MN, SB_VEC>>(p, status, stream, dev);
+}
+
+bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)
+{
+    return gm >= 1 && gn >= 128 && gk >= 128 && gn % 128 == 0 && gk % 128 == 0 && gm <= kMaxDim && gn <= kMaxDim &&
+           gk <= kMaxDim && (gm + 127) / 128 <= kMaxGridY;
+}
+
+}  // namespace
+}  // namespace bfp8
+
+using namespace bfp8;
+
+// =================================================================== quantisers
+extern "C" int fp8_quantize_act(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q, int64_t ldq,
+                                float* s, int64_t lds, void* stream)
+{
+    if (R < 0 || C < 0)
+        return BFP8_EINVAL;
+    if (C % 128 != 0 || R > kMaxDim || C > kMaxDim)
+        return BFP8_ESHAPE;
+    if (R == 0 || C == 0)
+        return BFP8_OK;
+    if (!x || !q || !s || ldx < C || ldq < C || lds < R)
+        return BFP8_EINVAL;
+    if (!aligned(x, 16) || ldx % 8 || !aligned(q, 8) || ldq % 8 || !aligned(s, 4))
+        return BFP8_EALIGN;
+    int rc = check_arch(nullptr);
+    if (rc != BFP8_OK)
+        return rc;
+    const int64_t nchunks = C / 128;
+    const int64_t ntiles = R * nchunks;
+    constexpr int UNROLL = 2;
+    const int64_t blocks = (ntiles + 16 * UNROLL - 1) / (16 * UNROLL);
+    quant_act_kernel<UNROLL><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), ldx, q, ldq, s, lds, nchunks, ntiles);
+    return launch_status();
+}
+
+extern "C" int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                                   float* s, void* stream)
+{
+    if (N < 0 || K < 0)
+        return BFP8_EINVAL;
+    if (N % 128 || K % 128 || N > kMaxDim || K > kMaxDim || N / 128 > kMaxGridY)
+        return BFP8_ESHAPE;
+    if (N == 0 || K == 0)
+        return BFP8_OK;
+    if (!w || !q || !s || ldw < K || ldq < K)
+        return BFP8_EINVAL;
+    if (!aligned(w, 16) || ldw % 8 || !aligned(q, 8) || ldq % 8 || !aligned(s, 4))
+        return BFP8_EALIGN;
+    int rc = check_arch(nullptr);
+    if (rc != BFP8_OK)
+        return rc;
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    quant_weight_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(w), ldw,
+                                                                             q, ldq, s, K / 128);
+    return launch_status();
+}
+
+extern "C" int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* qt,
+                                      int64_t ldqt, float* st, int64_t ldst, void* stream)
+{
+    if (R < 0 || C < 0)
+        return BFP8_EINVAL;
+    if (C % 128 || R > kMaxDim || C > kMaxDim || (R + 127) / 128 > kMaxGridY)
+        return BFP8_ESHAPE;
+    if (R == 0 || C == 0)
+        return BFP8_OK;
+    const int64_t R128 = (R + 127) / 128 * 128;
+    if (!x || !qt || !st || ldx < C || ldqt < R128 || ldst < C)
+        return BFP8_EINVAL;
+    if (!aligned(x, 16) || ldx % 8 || !aligned(qt, 16) || ldqt % 16 || !aligned(st, 8) || ldst % 2)
+        return BFP8_EALIGN;
+    int rc = check_arch(nullptr);
+    if (rc != BFP8_OK)
+        return rc;
+    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R128 / 128));
+    quant_transpose_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), R, ldx, qt, ldqt, st, ldst);
+    return launch_status();
+}
+
+// =================================================================== GEMMs
+extern "C" int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* sx, int64_t ldsx,
+                                  const uint8_t* qw, int64_t ldqw, const float* sw, void* y, int64_t ldy,
+                                  int64_t M, int64_t N, int64_t K, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return BFP8_EINVAL;
+    if (M == 0)
+        return (N % 128 || K % 128) ? BFP8_ESHAPE : BFP8_OK;
+    if (!gemm_dims_ok(M, N, K))
+        return BFP8_ESHAPE;
+    if (!qx || !sx || !qw || !sw || !y || ldqx < K || ldqw < K || ldsx < M || ldy < N)
+        return BFP8_EINVAL;
+    if (!aligned(qx, 16) || !aligned(qw, 16) || !aligned(sx, 16) || !aligned(y, 16) || !aligned(sw, 4) ||
+        ldqx % 16 || ldqw % 16 || ldsx % 4 || ldy % 8)
+        return BFP8_EALIGN;
+    GemmProblem p{};
+    p.a = qx;
+    p.lda = ldqx;
+    p.b = qw;
+    p.ldb = ldqw;
+    p.b_mn = false;
+    p.sa = sx;
+    p.ld_sa = ldsx;
+    p.sb = sw;
+    p.sb_vec = false;
+    p.sb_col_stride = K / 128;  // sw[n/128][kb]
+    p.sb_chunk_stride = 1;
+    p.d = y;
+    p.ldd = ldy;
+    p.gm = M;
+    p.gn = N;
+    p.gk = K;
+    return dispatch_gemm<false, false>(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const float* sdy, int64_t ldsdy,
+                                    const uint8_t* qw, int64_t ldqw, const float* sw, void* dx, int64_t lddx,
+                                    int64_t M, int64_t N, int64_t K, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return BFP8_EINVAL;
+    if (M == 0)
+        return (N % 128 || K % 128) ? BFP8_ESHAPE : BFP8_OK;
+    if (!gemm_dims_ok(M, K, N))
+        return BFP8_ESHAPE;
+    if (!qdy || !sdy || !qw || !sw || !dx || ldqdy < N || ldqw < K || ldsdy < M || lddx < K)
+        return BFP8_EINVAL;
+    if (!aligned(qdy, 16) || !aligned(qw, 16) || !aligned(sdy, 16) || !aligned(dx, 16) || !aligned(sw, 4) ||
+        ldqdy % 16 || ldqw % 16 || ldsdy % 4 || lddx % 8)
+        return BFP8_EALIGN;
+    GemmProblem p{};
+    p.a = qdy;
+    p.lda = ldqdy;
+    p.b = qw;  // [N][K]: contraction (N) strided, output columns (K) contiguous
+    p.ldb = ldqw;
+    p.b_mn = true;
+    p.sa = sdy;
+    p.ld_sa = ldsdy;
+    p.sb = sw;
+    p.sb_vec = false;
+    p.sb_col_stride = 1;  // sw[nb][k/128]
+    p.sb_chunk_stride = K / 128;
+    p.d = dx;
+    p.ldd = lddx;
+    p.gm = M;
+    p.gn = K;
+    p.gk = N;
+    return dispatch_gemm<true, false>(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
+                                    const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt, void* dw,
+                                    int64_t lddw, int64_t M, int64_t N, int64_t K, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return BFP8_EINVAL;
+    const int64_t M128 = (M + 127) / 128 * 128;
+    if (M < 1 || !gemm_dims_ok(N, K, M128))
+        return BFP8_ESHAPE;
+    if (!qdyt || !sdyt || !qxt || !sxt || !dw || ldqdyt < M128 || ldqxt < M128 || ldsdyt < N || ldsxt < K ||
+        lddw < K)
+        return BFP8_EINVAL;
+    if (!aligned(qdyt, 16) || !aligned(qxt, 16) || !aligned(sdyt, 16) || !aligned(sxt, 16) || !aligned(dw, 16) ||
+        ldqdyt % 16 || ldqxt % 16 || ldsdyt % 4 || ldsxt % 4 || lddw % 8)
+        return BFP8_EALIGN;
+    GemmProblem p{};
+    p.a = qdyt;
+    p.lda = ldqdyt;
+    p.b = qxt;
+    p.ldb = ldqxt;
+    p.b_mn = false;
+    p.sa = sdyt;
+    p.ld_sa = ldsdyt;
+    p.sb = sxt;
+    p.ld_sb = ldsxt;
+    p.sb_vec = true;
+    p.d = dw;
+    p.ldd = lddw;
+    p.gm = N;
+    p.gn = K;
+    p.gk = M128;
+    return dispatch_gemm<false, true>(p, static_cast<cudaStream_t>(stream));
+}
+
+// =================================================================== misc
+extern "C" const char* bfp8_status_string(int status)
+{
+    switch (status) {
+    case BFP8_OK:
+        return "BFP8_OK";
+    case BFP8_EINVAL:
+        return "BFP8_EINVAL: null pointer, negative size or leading dimension too small";
+    case BFP8_EALIGN:
+        return "BFP8_EALIGN: pointer or leading dimension breaks a 16-byte alignment rule";
+    case BFP8_ESHAPE:
+        return "BFP8_ESHAPE: dimension not a multiple of 128, or too large";
+    case BFP8_ELAUNCH:
+        return "BFP8_ELAUNCH: CUDA launch or tensor-map encoding failed";
+    case BFP8_ETIMEOUT:
+        return "BFP8_ETIMEOUT: a kernel gave up on a bounded wait";
+    case BFP8_EARCH:
+        return "BFP8_EARCH: device is not compute capability 10.3 (sm_103)";
+    default:
+        return "unknown bfp8 status";
+    }
+}
+
+extern "C" int bfp8_last_device_status(void* stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return BFP8_ELAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned host = 0, zero = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return BFP8_ELAUNCH;
+    if (cudaMemcpyFromSymbolAsync(&host, g_device_status, sizeof host, 0, cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return BFP8_ELAUNCH;
+    return (host & kDevTimeout) ? BFP8_ETIMEOUT : BFP8_OK;
+}
+
+extern "C" int bfp8_set_gemm_tile_n(int tile_n)
+{
+    if (tile_n != 0 && tile_n != 128 && tile_n != 256)
+        return BFP8_EINVAL;
+    return g_tile_n.exchange(tile_n);
+}

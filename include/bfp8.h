@@ -1,0 +1,134 @@
+/*
+ * bfp8.h — C ABI of the blockwise-FP8 linear-layer library for B300 (sm_103a).
+ *
+ * What the library computes. The Puro-2B pretraining recipe runs the matrix
+ * multiplications of its main linear layers in FP8, "following DeepSeek-V3's
+ * fine-grained block quantisation", and keeps numerically sensitive work and
+ * training state in BF16/FP32 (Puro-2B article on en.roboind.com, section
+ * "FP8 takes advantage of the RTX 5090's low precision efficiency"; the
+ * ainews.surl.tw article "Puro-2B Publishes a Consumer-Grade GPU Pretraining
+ * Recipe ..." names it "blockwise FP8"). The pages fix no further detail; this
+ * library adopts the DeepSeek-V3 convention:
+ *   - activation tiles of 1x128 along the contraction axis, weight blocks of
+ *     128x128;
+ *   - codes in OCP E4M3FN (largest finite value 448);
+ *   - one FP32 scale per tile: s = fl32(amax / 448), IEEE division;
+ *   - code = e4m3_rn_satfinite(fl32(x / s)), IEEE division, then round to
+ *     nearest-even with saturation to +-448; an all-zero tile has s = 0 and
+ *     signed-zero codes (0x00 / 0x80 by the input's sign);
+ *   - GEMMs: FP8 tensor-core products summed in FP32 per 128-wide chunk of the
+ *     contraction axis, each chunk promoted into an FP32 accumulator with the
+ *     product of its two scales; BF16 output, rounded to nearest-even.
+ * A linear layer y = x W^T (x [M,K], W [N,K]) uses six calls per training
+ * step: fp8_quantize_act(x), fp8_quantize_weight(W), fp8_block_gemm_fwd;
+ * fp8_quantize_act(dy), fp8_block_gemm_dgrad; fp8_quantize_transpose(dy),
+ * fp8_quantize_transpose(x), fp8_block_gemm_wgrad.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers on the current CUDA device, owned and
+ *     allocated by the caller. The library allocates nothing, frees nothing
+ *     and never synchronises (except bfp8_last_device_status).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous on that stream.
+ *   - Matrices are row-major; ld* arguments are row strides in ELEMENTS.
+ *   - BF16 arrays are passed as void* holding IEEE bfloat16 bit patterns.
+ *   - Arguments are checked on the host before any launch. Return value:
+ *     BFP8_OK, or a negative bfp8_status; nothing is launched on error.
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified codes.
+ *   - Outputs must not overlap inputs or each other.
+ */
+#ifndef BFP8_H
+#define BFP8_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BFP8_OK = 0,
+    BFP8_EINVAL = -1,   /* null pointer, negative size, leading dimension too small */
+    BFP8_EALIGN = -2,   /* pointer or leading dimension breaks a 16-byte (TMA / vector) rule */
+    BFP8_ESHAPE = -3,   /* a dimension that must be a multiple of 128 is not, or is too large */
+    BFP8_ELAUNCH = -4,  /* the CUDA launch (or tensor-map encoding) failed */
+    BFP8_ETIMEOUT = -5, /* a kernel gave up on a bounded wait (from bfp8_last_device_status) */
+    BFP8_EARCH = -6     /* the current device is not compute capability 10.3 (sm_103) */
+} bfp8_status;
+
+/* Activation quantiser: 1x128 tiles along the columns.
+ *   x [R][C] bf16 (ldx), C a multiple of 128, R >= 0 (R = 0 is a no-op).
+ *   q [R][C] E4M3 codes (ldq), s [C/128][R] FP32 scales, chunk-major (lds >= R).
+ * Used for x in the forward pass (tiles along K) and for dy in the input-
+ * gradient pass (tiles along N).
+ * Alignment: x 16 B and ldx % 8 == 0; q 8 B and ldq % 8 == 0; s 4 B. */
+int fp8_quantize_act(const void* x, int64_t R, int64_t C, int64_t ldx,
+                     uint8_t* q, int64_t ldq, float* s, int64_t lds, void* stream);
+
+/* Weight quantiser: 128x128 blocks.
+ *   w [N][K] bf16 (ldw), N and K multiples of 128.
+ *   q [N][K] E4M3 codes (ldq), s [N/128][K/128] FP32 scales, dense.
+ * The same codes and scales serve the forward and the input-gradient GEMM.
+ * Alignment: w 16 B and ldw % 8 == 0; q 8 B and ldq % 8 == 0; s 4 B. */
+int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw,
+                        uint8_t* q, int64_t ldq, float* s, void* stream);
+
+/* Transposed activation quantiser (operands of the weight-gradient GEMM):
+ * 1x128 tiles run down the columns of x, i.e. along the R rows (tokens), and
+ * the codes are written transposed.
+ *   x [R][C] bf16 (ldx), C a multiple of 128, R >= 0; R128 = R rounded up to 128.
+ *   qt [C][R128] E4M3 codes (ldqt >= R128); pad columns R..R128-1 get 0x00.
+ *   st [R128/128][C] FP32 scales (ldst >= C); a chunk's scale covers its valid rows.
+ * Alignment: x 16 B and ldx % 8 == 0; qt 16 B and ldqt % 16 == 0;
+ * st 8 B and ldst % 2 == 0. */
+int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64_t ldx,
+                           uint8_t* qt, int64_t ldqt, float* st, int64_t ldst, void* stream);
+
+/* Forward GEMM, y = x W^T:
+ *   y[m][n] = bf16( sum_kb sx[kb][m] * sw[n/128][kb] * sum_{k in kb} qx[m][k] qw[n][k] )
+ *   qx [M][K] (ldqx), sx [K/128][M] (ldsx), qw [N][K] (ldqw), sw [N/128][K/128] dense,
+ *   y [M][N] bf16 (ldy). K, N multiples of 128; M >= 0 any (M = 0 is a no-op).
+ * Alignment: qx, qw, sx, y 16 B; ldqx, ldqw % 16 == 0; ldsx % 4 == 0; ldy % 8 == 0. */
+int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* sx, int64_t ldsx,
+                       const uint8_t* qw, int64_t ldqw, const float* sw,
+                       void* y, int64_t ldy, int64_t M, int64_t N, int64_t K, void* stream);
+
+/* Input-gradient GEMM, dx = dy W (contraction over the layer's N outputs):
+ *   dx[m][k] = bf16( sum_nb sdy[nb][m] * sw[nb][k/128] * sum_{n in nb} qdy[m][n] qw[n][k] )
+ *   qdy [M][N] (ldqdy), sdy [N/128][M] (ldsdy), qw/sw exactly as produced for the
+ *   forward pass (qw is read with the contraction axis strided), dx [M][K] bf16 (lddx).
+ * Alignment: as fp8_block_gemm_fwd. */
+int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const float* sdy, int64_t ldsdy,
+                         const uint8_t* qw, int64_t ldqw, const float* sw,
+                         void* dx, int64_t lddx, int64_t M, int64_t N, int64_t K, void* stream);
+
+/* Weight-gradient GEMM, dW = dy^T x (contraction over the M tokens, padded
+ * with zero codes to M128):
+ *   dw[n][k] = bf16( sum_mb sdyt[mb][n] * sxt[mb][k] * sum_{m in mb} qdyt[n][m] qxt[k][m] )
+ *   qdyt [N][M128] (ldqdyt), sdyt [M128/128][N] (ldsdyt), qxt [K][M128] (ldqxt),
+ *   sxt [M128/128][K] (ldsxt), all from fp8_quantize_transpose; dw [N][K] bf16 (lddw).
+ *   M >= 1 any; N, K multiples of 128.
+ * Alignment: qdyt, qxt, sdyt, sxt, dw 16 B; ldqdyt, ldqxt % 16 == 0;
+ * ldsdyt, ldsxt % 4 == 0; lddw % 8 == 0. */
+int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
+                         const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
+                         void* dw, int64_t lddw, int64_t M, int64_t N, int64_t K, void* stream);
+
+/* Human-readable name of a bfp8_status value (static string, never NULL). */
+const char* bfp8_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the device status word that a
+ * kernel sets when it gives up on a bounded wait. Returns BFP8_OK,
+ * BFP8_ETIMEOUT, or BFP8_ELAUNCH if the synchronisation itself failed. */
+int bfp8_last_device_status(void* stream);
+
+/* Tuning knob for the GEMMs' output tile width: 0 = automatic (default),
+ * 128 or 256 columns. Returns the previous setting, or BFP8_EINVAL. Applies
+ * to later calls from every thread. */
+int bfp8_set_gemm_tile_n(int tile_n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BFP8_H */

@@ -1,0 +1,82 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/bfp8.h declares, and rejects bad arguments on the host before any CUDA
+call (no launch happens for these cases, so they are safe anywhere)."""
+import ctypes
+
+import pytest
+
+import blockwise_fp8_linear_weight_b300 as bfp8
+from blockwise_fp8_linear_weight_b300 import build as bfp8_build
+
+OK, EINVAL, EALIGN, ESHAPE = 0, -1, -2, -3
+A = 0x10000  # a 16-byte-aligned fake device address; never dereferenced in these cases
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bfp8_build.build()
+    return bfp8.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = bfp8.header_functions()
+    assert set(names) >= {"fp8_quantize_act", "fp8_quantize_weight", "fp8_quantize_transpose",
+                          "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
+                          "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n"}
+    cdll = ctypes.CDLL(bfp8.LIB_PATH)
+    for n in names:
+        assert hasattr(cdll, n), n
+
+
+def test_status_strings(lib):
+    for code, name in bfp8.STATUS.items():
+        assert lib.bfp8_status_string(code).decode().startswith(name)
+    assert lib.bfp8_status_string(12345) == b"unknown bfp8 status"
+
+
+def test_tile_knob(lib):
+    assert lib.bfp8_set_gemm_tile_n(64) == EINVAL
+    prev = lib.bfp8_set_gemm_tile_n(256)
+    assert lib.bfp8_set_gemm_tile_n(prev) == 256
+
+
+def test_quantiser_argument_checks(lib):
+    s = None
+    # C not a multiple of 128
+    assert lib.fp8_quantize_act(A, 4, 100, 128, A, 128, A, 4, s) == ESHAPE
+    # empty input is a no-op
+    assert lib.fp8_quantize_act(None, 0, 128, 128, None, 128, None, 0, s) == OK
+    assert lib.fp8_quantize_act(A, -1, 128, 128, A, 128, A, 4, s) == EINVAL
+    # null output, short leading dimension
+    assert lib.fp8_quantize_act(A, 4, 128, 128, None, 128, A, 4, s) == EINVAL
+    assert lib.fp8_quantize_act(A, 4, 256, 128, A, 256, A, 4, s) == EINVAL
+    assert lib.fp8_quantize_act(A, 8, 128, 128, A, 128, A, 4, s) == EINVAL  # lds < R
+    # misaligned input pointer / row stride
+    assert lib.fp8_quantize_act(A + 2, 4, 128, 128, A, 128, A, 4, s) == EALIGN
+    assert lib.fp8_quantize_act(A, 4, 128, 132, A, 128, A, 4, s) == EALIGN
+    assert lib.fp8_quantize_weight(A, 100, 128, 128, A, 128, A, s) == ESHAPE
+    assert lib.fp8_quantize_weight(A, 128, 128, 128, A + 4, 128, A, s) == EALIGN
+    assert lib.fp8_quantize_transpose(A, 4, 120, 128, A, 128, A, 128, s) == ESHAPE
+    assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 200, A, 128, s) == EINVAL  # ldqt < R128
+    assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 264, A, 128, s) == EALIGN  # ldqt % 16
+    assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 256, A + 4, 128, s) == EALIGN
+
+
+def test_gemm_argument_checks(lib):
+    s = None
+    # fwd: N, K multiples of 128
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 130, 128, s) == ESHAPE
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 96, s) == ESHAPE
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 0, 128, 128, s) == OK
+    assert lib.fp8_block_gemm_fwd(None, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, s) == EINVAL
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 3, A, 128, A, A, 128, 4, 128, 128, s) == EINVAL  # ldsx < M
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 6, A, 128, A, A, 128, 6, 128, 128, s) == EALIGN  # ldsx % 4
+    assert lib.fp8_block_gemm_fwd(A, 136, A, 4, A, 136, A, A, 128, 4, 128, 128, s) == EALIGN  # ldq % 16
+    assert lib.fp8_block_gemm_fwd(A, 128, A + 4, 4, A, 128, A, A, 128, 4, 128, 128, s) == EALIGN
+    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 96, A, A, 96, 4, 128, 96, s) == ESHAPE
+    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 128, A, A, 100, 4, 128, 128, s) == EINVAL
+    # wgrad: M >= 1, ld of transposed codes >= M128
+    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 0, 128, 128, s) == ESHAPE
+    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 200, 128, 128, s) == EINVAL
+    assert lib.fp8_block_gemm_wgrad(A, 256, A, 126, A, 256, A, 128, A, 128, 200, 128, 128, s) == EINVAL
+    assert lib.fp8_block_gemm_wgrad(A, 256, A, 130, A, 256, A, 128, A, 128, 200, 128, 128, s) == EALIGN

@@ -1,0 +1,149 @@
+"""GPU parity of the three blockwise-FP8 GEMMs against the FP64 oracle.
+
+Every input comes from the seeded generators or from the oracle's own
+quantisers (never from the CUDA path). Bar, on every compared element:
+    |y - y_ref| <= 1e-2 |y_ref| + 1e-3 rms(y_ref)
+with y_ref the oracle's FP64 result from the same codes and scales and rms over
+the compared output (the whole matrix for small shapes, the sampled rows at
+full size). Small shapes are compared in full and span several tiles and a
+ragged tail; the Puro-2B workload shapes are compared on sampled rows (all
+columns), in the launch configuration the benchmark uses."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import from_dev_bf16, gemm_tolerance_ok, sample_rows, scales_to_dev, to_dev
+
+import blockwise_fp8_linear_weight_b300 as bfp8
+
+pytestmark = pytest.mark.gpu
+TILE = 128
+
+
+@pytest.fixture(params=[128], ids=lambda t: f"tileN{t}")
+def tile_n(request):
+    prev = bfp8.set_gemm_tile_n(request.param)
+    yield request.param
+    bfp8.set_gemm_tile_n(prev)
+
+
+def _check(y_gpu, y_ref, what):
+    ok, ratio = gemm_tolerance_ok(y_gpu, y_ref)
+    assert ok, f"{what}: worst error/allowance = {ratio:.3g}"
+
+
+# ------------------------------------------------------------------ per-pass runners
+def run_fwd(qx, sx, qw, sw, rows=None):
+    y = bfp8.fp8_block_gemm_fwd(to_dev(qx), scales_to_dev(sx), to_dev(qw), to_dev(sw))
+    torch.cuda.synchronize()
+    y = from_dev_bf16(y)
+    ref = oracle.gemm_fwd(qx, sx, qw, sw, rows=rows)
+    return (y if rows is None else y[rows]), ref
+
+
+def run_dgrad(qdy, sdy, qw, sw, rows=None):
+    dx = bfp8.fp8_block_gemm_dgrad(to_dev(qdy), scales_to_dev(sdy), to_dev(qw), to_dev(sw))
+    torch.cuda.synchronize()
+    dx = from_dev_bf16(dx)
+    ref = oracle.gemm_dgrad(qdy, sdy, qw, sw, rows=rows)
+    return (dx if rows is None else dx[rows]), ref
+
+
+def run_wgrad(qdyt, sdyt, qxt, sxt, M, rows=None):
+    dw = bfp8.fp8_block_gemm_wgrad(to_dev(qdyt), scales_to_dev(sdyt), to_dev(qxt), scales_to_dev(sxt), M)
+    torch.cuda.synchronize()
+    dw = from_dev_bf16(dw)
+    ref = oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, M, rows=rows)
+    return (dw if rows is None else dw[rows]), ref
+
+
+# ------------------------------------------------------------------ random codes and scales
+SMALL = [(1, 128, 128), (5, 256, 128), (128, 128, 256), (200, 384, 640), (256, 256, 256), (300, 512, 384),
+         (129, 640, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_fwd_random_codes(tile_n, M, N, K):
+    qx = wl.random_codes((M, K), 1)
+    sx = wl.random_scales((K // TILE, M), 2)
+    qw = wl.random_codes((N, K), 3)
+    sw = wl.random_scales((N // TILE, K // TILE), 4)
+    _check(*run_fwd(qx, sx, qw, sw), "fwd")
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_dgrad_random_codes(tile_n, M, N, K):
+    qdy = wl.random_codes((M, N), 5)
+    sdy = wl.random_scales((N // TILE, M), 6)
+    qw = wl.random_codes((N, K), 7)
+    sw = wl.random_scales((N // TILE, K // TILE), 8)
+    _check(*run_dgrad(qdy, sdy, qw, sw), "dgrad")
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_wgrad_random_codes(tile_n, M, N, K):
+    M128 = (M + TILE - 1) // TILE * TILE
+    qdyt = wl.random_codes((N, M128), 9)
+    qxt = wl.random_codes((K, M128), 10)
+    qdyt[:, M:] = 0
+    qxt[:, M:] = 0
+    sdyt = wl.random_scales((M128 // TILE, N), 11)
+    sxt = wl.random_scales((M128 // TILE, K), 12)
+    _check(*run_wgrad(qdyt, sdyt, qxt, sxt, M), "wgrad")
+
+
+def test_zero_scale_chunks_and_single_chunk(tile_n):
+    """All-zero tiles (scale 0) contribute nothing; a lone non-zero chunk is one dot product."""
+    M, N, K = 130, 256, 512
+    qx = wl.random_codes((M, K), 21)
+    sx = wl.random_scales((K // TILE, M), 22)
+    sx[1, :] = 0.0
+    qx[:, 2 * TILE:3 * TILE] = 0
+    qw = wl.random_codes((N, K), 23)
+    sw = wl.random_scales((N // TILE, K // TILE), 24)
+    _check(*run_fwd(qx, sx, qw, sw), "fwd with zero chunks")
+
+
+# ------------------------------------------------------------------ quantise (oracle) then GEMM
+def _linear_case(lin, rows_m=None, rows_n=None):
+    x, w, dy = wl.make_linear(lin)
+    qx, sx = oracle.quantize_act(x)
+    qw, sw = oracle.quantize_weight(w)
+    qdy, sdy = oracle.quantize_act(dy)
+    qdyt, sdyt = oracle.quantize_transpose(dy)
+    qxt, sxt = oracle.quantize_transpose(x)
+    _check(*run_fwd(qx, sx, qw, sw, rows_m), f"{lin.name} fwd")
+    _check(*run_dgrad(qdy, sdy, qw, sw, rows_m), f"{lin.name} dgrad")
+    _check(*run_wgrad(qdyt, sdyt, qxt, sxt, lin.M, rows_n), f"{lin.name} wgrad")
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 256, 256), (1000, 512, 384), (333, 256, 640)])
+def test_quantised_linear_small_full_compare(tile_n, M, K, N):
+    _linear_case(wl.Linear("small", M, K, N, "student_t3", M))
+
+
+def test_single_linear_256_config(tile_n):
+    """One linear, forward only: X [256,256] ~ N(0,1), W [256,256] ~ N(0, 0.02^2), seed 0; full compare."""
+    lin = wl.single_linear_256().linears[0]
+    x, w, _ = wl.make_linear(lin)
+    qx, sx = oracle.quantize_act(x)
+    qw, sw = oracle.quantize_weight(w)
+    _check(*run_fwd(qx, sx, qw, sw), "single linear fwd")
+
+
+def _full_size_cases():
+    cases = list(wl.attention_projections().linears) + list(wl.mlp_projections().linears)
+    cases += list(wl.full_stack(layers=1).linears)
+    return cases
+
+
+@pytest.mark.parametrize("lin", _full_size_cases(), ids=lambda l: f"{l.name}-M{l.M}-K{l.K}-N{l.N}")
+def test_workload_shapes_sampled_rows(lin):
+    _linear_case(lin, sample_rows(lin.M, 48, lin.M + lin.N), sample_rows(lin.N, 32, lin.K))
+
+
+@pytest.mark.parametrize("lin", wl.shape_sweep(), ids=lambda l: l.name)
+def test_shape_sweep_sampled_rows(lin):
+    _linear_case(lin, sample_rows(lin.M, 24, lin.M + lin.N), sample_rows(lin.N, 16, lin.K))

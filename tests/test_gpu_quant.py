@@ -1,0 +1,138 @@
+"""GPU parity of the three quantisers: E4M3 codes and FP32 scales must equal the
+oracle's bit for bit, on edge cases (ragged rows, zero tiles, signed zeros,
+subnormal scales, huge values) and on the full-size Puro-2B workload tensors."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import to_dev_bf16
+
+import blockwise_fp8_linear_weight_b300 as bfp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_act(bits):
+    q, s = bfp8.fp8_quantize_act(to_dev_bf16(bits))
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+def _gpu_weight(bits):
+    q, s = bfp8.fp8_quantize_weight(to_dev_bf16(bits))
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+def _gpu_transpose(bits):
+    qt, st = bfp8.fp8_quantize_transpose(to_dev_bf16(bits))
+    torch.cuda.synchronize()
+    return qt.cpu().numpy(), st.cpu().numpy()
+
+
+def _same(a, b):
+    assert a.shape == b.shape
+    if a.dtype == np.float32:
+        a, b = a.view(np.uint32), b.view(np.uint32)
+    bad = np.argwhere(a != b)
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+def _special_input(R, C, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((R, C)).astype(np.float32)
+    if R >= 6:
+        x[0, :] = 0.0                                    # all-zero tiles
+        x[1, :] = -0.0                                   # signed zeros
+        x[2, :] *= 1e-39                                 # bf16 subnormals -> tiny scales
+        x[3, :] *= 3e38 / np.abs(x[3]).max()             # near the top of the range
+        x[4, ::7] = 0.0
+        x[5, :] = np.where(rng.random(C) < 0.5, -1.0, 1.0) * np.ldexp(1.0, rng.integers(-20, 20, C))
+    return wl.bf16_bits(x)
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (6, 256), (37, 384), (128, 128), (300, 640), (1000, 2048)])
+def test_act_edge_shapes(R, C):
+    x = _special_input(R, C, R + C)
+    q, s = _gpu_act(x)
+    qo, so = oracle.quantize_act(x)
+    _same(q, qo)
+    _same(s, so)
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 384), (384, 256)])
+def test_weight_edge_shapes(N, K):
+    w = _special_input(N, K, N * K)
+    q, s = _gpu_weight(w)
+    qo, so = oracle.quantize_weight(w)
+    _same(q, qo)
+    _same(s, so)
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (6, 256), (127, 128), (128, 256), (129, 128), (300, 384), (1000, 2048)])
+def test_transpose_edge_shapes(R, C):
+    x = _special_input(R, C, 7 * R + C)
+    qt, st = _gpu_transpose(x)
+    qo, so = oracle.quantize_transpose(x)
+    _same(qt, qo)
+    _same(st, so)
+
+
+def test_zero_rows_and_student_t():
+    rng = np.random.default_rng(3)
+    x = wl.bf16_bits(rng.standard_t(3, size=(257, 1024)).astype(np.float32))
+    for f in (_gpu_act, _gpu_transpose):
+        a = f(x)
+        b = oracle.quantize_act(x) if f is _gpu_act else oracle.quantize_transpose(x)
+        _same(a[0], b[0])
+        _same(a[1], b[1])
+
+
+def _workload_tensors():
+    out = []
+    for lin in wl.attention_projections().linears + wl.mlp_projections().linears:
+        out.append(lin)
+    # one layer of the full stack (every layer has the same shapes), outlier-channel inputs
+    out.extend(wl.full_stack(layers=1).linears)
+    return out
+
+
+@pytest.mark.parametrize("lin", _workload_tensors(), ids=lambda l: f"{l.name}-M{l.M}-K{l.K}-N{l.N}")
+def test_full_size_workload_tensors(lin):
+    x, w, dy = wl.make_linear(lin)
+    for bits in (x, dy):
+        q, s = _gpu_act(bits)
+        qo, so = oracle.quantize_act(bits)
+        _same(q, qo)
+        _same(s, so)
+        qt, st = _gpu_transpose(bits)
+        qo, so = oracle.quantize_transpose(bits)
+        _same(qt, qo)
+        _same(st, so)
+    q, s = _gpu_weight(w)
+    qo, so = oracle.quantize_weight(w)
+    _same(q, qo)
+    _same(s, so)
+
+
+def test_strided_inputs_and_outputs():
+    """Leading dimensions larger than the row length on every argument."""
+    x = wl.random_bits((100, 384), seed=9)
+    xd = torch.zeros((100, 512), dtype=torch.bfloat16, device="cuda")
+    xd[:, :384] = to_dev_bf16(x)
+    q = torch.full((100, 400), 0xAB, dtype=torch.uint8, device="cuda")
+    s = torch.full((3, 104), -1.0, dtype=torch.float32, device="cuda")
+    bfp8.fp8_quantize_act(xd[:, :384], q[:, :384], s[:, :100])
+    qo, so = oracle.quantize_act(x)
+    _same(q[:, :384].cpu().numpy(), qo)
+    _same(s[:, :100].cpu().numpy(), so)
+    assert (q[:, 384:].cpu().numpy() == 0xAB).all() and (s[:, 100:].cpu().numpy() == -1.0).all()
+    qt = torch.full((384, 160), 0xCD, dtype=torch.uint8, device="cuda")
+    st = torch.full((1, 390), -1.0, dtype=torch.float32, device="cuda")
+    bfp8.fp8_quantize_transpose(xd[:, :384], qt[:, :128], st[:, :384])
+    qo, so = oracle.quantize_transpose(x)
+    _same(qt[:, :128].cpu().numpy(), qo)
+    _same(st[:, :384].cpu().numpy(), so)
+    assert (qt[:, 128:].cpu().numpy() == 0xCD).all()
