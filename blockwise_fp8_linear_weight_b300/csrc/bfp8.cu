@@ -68,6 +68,19 @@ unsigned* device_status_ptr(int dev)
     return p;
 }
 
+// Number of SMs of a device, cached (the persistent GEMM launches one CTA per SM).
+int sm_count(int dev)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -145,7 +158,7 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
                             CU_TENSOR_MAP_SWIZZLE_NONE);
     else
         tmSB = tmSA;  // unused in scalar mode
-    ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.d, p.gn, p.gm, p.ldd * 2, 64, 128,
+    ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.d, p.gn, p.gm, p.ldd * 2, 64, 32,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok)
         return BFP8_ELAUNCH;
@@ -162,12 +175,18 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     args.gm = static_cast<int>(p.gm);
     args.gn = static_cast<int>(p.gn);
     args.num_chunks = static_cast<int>(nc);
+    args.tiles_m = static_cast<int>((p.gm + Cfg::BM - 1) / Cfg::BM);
+    args.tiles_n = static_cast<int>((p.gn + Cfg::BN - 1) / Cfg::BN);
+    // sweep along N first when B is the smaller operand (it then stays in L2
+    // while the larger A is streamed once), along M otherwise
+    args.n_fastest = p.gn < p.gm ? 1 : 0;
     args.sb_scalar = p.sb;
     args.sb_col_stride = p.sb_col_stride;
     args.sb_chunk_stride = p.sb_chunk_stride;
     args.status = status;
-    dim3 grid(static_cast<unsigned>((p.gn + Cfg::BN - 1) / Cfg::BN), static_cast<unsigned>((p.gm + 127) / 128));
-    kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
+    const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
+    const int ctas = static_cast<int>(tiles < sm_count(dev) ? tiles : sm_count(dev));
+    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
     return launch_status();
 }
 
@@ -183,10 +202,10 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
         return BFP8_ELAUNCH;
     int tn = g_tile_n.load(std::memory_order_relaxed);
     if (tn == 0)
-        tn = 128;
+        tn = 256;
     if (tn == 256)
-        return run_gemm<GemmConfig<256, 4, B_MN, SB_VEC>>(p, status, stream, dev);
-    return run_gemm<GemmConfig<128, 6, B_MN, SB_VEC>>(p, status, stream, dev);
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC>>(p, status, stream, dev);
+    return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
 }
 
 bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)

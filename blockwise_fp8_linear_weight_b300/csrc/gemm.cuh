@@ -12,20 +12,28 @@
 // accumulated by the tensor core in FP32, then promoted into an FP32 register
 // accumulator with the product of the two chunk scales.
 //
-// Structure (one 128 x BN output tile per CTA):
-//   warp 0      TMA producer: A tile 128x128, B tile BNx128 (K-major) or
-//               128xBN (MN-major), the chunk's A scales (and B scales in vector
-//               mode) into a STAGES-deep shared-memory ring;
+// Persistent kernel, one CTA per SM, output tiles of 128 x BN visited in a
+// static round-robin order (the smaller operand is re-read from L2, the larger
+// one streamed once). Warp roles:
+//   warp 0      TMA producer: per chunk the A tile 128x128, the B tile (BNx128
+//               K-major, or 128-column boxes of an MN-major operand), the A
+//               scales and, in vector mode, the B scales, into a STAGES-deep
+//               shared-memory ring;
 //   warp 1      allocates TMEM; one thread issues 4 tcgen05.mma (K = 32 each)
-//               per chunk into one of two TMEM accumulators (double buffer);
-//   warps 4..   promotion: each warp owns 32 TMEM lanes (= 32 output rows) and
-//               128 columns; per chunk it loads the partial sums with
-//               tcgen05.ld, frees the TMEM buffer and does
-//               acc = fma(partial, sA * sB, acc) in registers; at the end the
-//               accumulators are rounded to BF16, staged in shared memory
-//               (128-byte swizzle) and written with TMA stores (rows or columns
-//               outside D are dropped by the TMA unit).
-// Every mbarrier wait is bounded (see mbar_wait); a timeout sets the library's
+//               per chunk into one of two TMEM accumulators of BN columns;
+//   warps 4..11 promotion: warp w owns TMEM lanes 32 (w%4) .. +31 (output rows)
+//               and BN/2 columns; per chunk it reads the partial sums with
+//               tcgen05.ld (two loads in flight per wait), releases the TMEM
+//               buffer and accumulates  acc += partial * (sA * sB)  in FP32
+//               registers; after the last chunk of a tile it rounds acc
+//               to BF16, stages it in its own 128-byte-swizzled shared-memory
+//               slab and issues TMA stores (the TMA unit drops rows and columns
+//               outside D), overlapping the MMAs of the next tile.
+// With BN = 256 the promotion warps need more than the 168 registers a
+// 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
+// warpgroup (40 each) to the promotion warpgroups (232 each):
+// 128 x 40 + 256 x 232 = 384 x 168.
+// Every mbarrier wait is bounded (mbar_wait); a timeout sets the library's
 // device status word and the kernel unwinds without hanging.
 #pragma once
 
@@ -43,38 +51,58 @@ struct GemmConfig {
     static constexpr int STAGES = STAGES_;
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
-    static constexpr int PROMO_WG = BN / 128;
-    static constexpr int PROMO_WARPS = 4 * PROMO_WG;
+    static constexpr int PROMO_WARPS = 8;
+    static constexpr int CPW = BN / 2;       // output columns per promotion warp
     static constexpr int THREADS = 128 + 32 * PROMO_WARPS;
+    static constexpr bool REG_SPLIT = (BN == 256);
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SA_BYTES = BM * 4;
     static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;
     static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + SA_BYTES + SB_BYTES;
+    // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 64 bf16 (4 KB, 128-byte swizzle)
+    static constexpr int BOX_BYTES = 32 * 128;
+    static constexpr int STAGE_OUT_BYTES = PROMO_WARPS * (CPW / 64) * BOX_BYTES;
     // shared-memory layout (offsets from a 1024-byte-aligned base)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_SA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_OUT = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SA = OFF_OUT + STAGE_OUT_BYTES;
     static constexpr int OFF_SB = OFF_SA + STAGES * SA_BYTES;
     static constexpr int OFF_BAR = OFF_SB + STAGES * SB_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-    // epilogue staging (reuses the operand ring once the main loop is done):
-    // per promotion warpgroup two 64-column slabs of 128 rows x 128 bytes
-    static constexpr int SLAB_BYTES = 128 * 128;
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
-    static_assert(PROMO_WG * 2 * SLAB_BYTES <= STAGES * (A_BYTES + B_BYTES), "staging must fit in the ring");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(!REG_SPLIT || 128 * 40 + 256 * 232 <= THREADS * 168, "register split");
 };
 
 struct GemmArgs {
     int gm, gn, num_chunks;
+    int tiles_m, tiles_n;
+    int n_fastest;            // tile order: 1 = sweep the N tiles of a row block first
     const float* sb_scalar;   // scalar mode: sB(c, j) = sb_scalar[(j/128) * sb_col_stride + c * sb_chunk_stride]
     int64_t sb_col_stride, sb_chunk_stride;
     unsigned* status;
 };
+
+template <class Cfg>
+__device__ __forceinline__ void tile_origin(const GemmArgs& args, int t, int& m0, int& n0)
+{
+    const int id = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+    int mb, nb;
+    if (args.n_fastest) {
+        nb = id % args.tiles_n;
+        mb = id / args.tiles_n;
+    } else {
+        mb = id % args.tiles_m;
+        nb = id / args.tiles_m;
+    }
+    m0 = mb * Cfg::BM;
+    n0 = nb * Cfg::BN;
+}
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
@@ -86,6 +114,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem + Cfg::OFF_A;
     uint8_t* sB = smem + Cfg::OFF_B;
+    uint8_t* sOut = smem + Cfg::OFF_OUT;
     float* sSA = reinterpret_cast<float*>(smem + Cfg::OFF_SA);
     float* sSB = reinterpret_cast<float*>(smem + Cfg::OFF_SB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
@@ -99,9 +128,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * Cfg::BN;
-    const int m0 = blockIdx.y * Cfg::BM;
     const int nc = args.num_chunks;
+    const int total_tiles = args.tiles_m * args.tiles_n;
+    const int my_tiles = total_tiles > static_cast<int>(blockIdx.x)
+                             ? (total_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    const int my_chunks = my_tiles * nc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -133,13 +165,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
+    // The register split sits inside each role's branch so that the compiler
+    // allocates every role's code under that role's budget.
+    if (warp < 4) {
+        if (Cfg::REG_SPLIT)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             int issued = 0;
-            for (int c = 0; c < nc; ++c) {
-                const int s = c % Cfg::STAGES;
-                const uint32_t ph = (c / Cfg::STAGES) & 1;
+            int t = 0, c = 0, m0 = 0, n0 = 0;
+            tile_origin<Cfg>(args, 0, m0, n0);
+            for (int g = 0; g < my_chunks; ++g) {
+                const int s = g % Cfg::STAGES;
+                const uint32_t ph = (g / Cfg::STAGES) & 1;
                 if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status))
                     break;
                 mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
@@ -156,11 +195,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (Cfg::SB_VEC)
                     tma_load_2d(sSB + s * Cfg::BN, &tmSB, &full[s], n0, c);
                 ++issued;
+                if (++c == nc) {
+                    c = 0;
+                    ++t;
+                    tile_origin<Cfg>(args, t, m0, n0);
+                }
             }
             // make sure no copy is still landing in shared memory before exit
-            for (int c = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; c < issued; ++c) {
+            for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g) {
                 volatile int never = 0;
-                mbar_wait(&full[c % Cfg::STAGES], (c / Cfg::STAGES) & 1, &never, args.status);
+                mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status);
             }
         }
     } else if (warp == 1) {
@@ -169,11 +213,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::BM, Cfg::BN, Cfg::B_MN);
             const uint32_t a_base = smem_u32(sA);
             const uint32_t b_base = smem_u32(sB);
-            for (int c = 0; c < nc; ++c) {
-                const int s = c % Cfg::STAGES;
-                const uint32_t ph = (c / Cfg::STAGES) & 1;
-                const int b = c & 1;
-                const uint32_t bph = (c >> 1) & 1;
+            for (int g = 0; g < my_chunks; ++g) {
+                const int s = g % Cfg::STAGES;
+                const uint32_t ph = (g / Cfg::STAGES) & 1;
+                const int b = g & 1;
+                const uint32_t bph = (g >> 1) & 1;
                 if (!mbar_wait(&full[s], ph, abort_flag, args.status))
                     break;
                 if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, args.status))
@@ -196,104 +240,130 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             volatile int never = 0;
             mbar_wait(mma_done, 0, &never, args.status);
         }
-    } else if (warp >= 4) {
+    }
+    } else {
+        if (Cfg::REG_SPLIT)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
         // ---------------------------------------------------------------- promotion + epilogue
-        const int pw = warp - 4;            // 0 .. PROMO_WARPS-1
-        const int g = pw >> 2;              // which 128-column half of the tile
+        constexpr int CPW = Cfg::CPW;
+        const int pw = warp - 4;            // 0 .. 7
+        const int half = pw >> 2;           // which half of the tile's columns
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
-        const int col0 = n0 + g * 128;      // first output column of this warpgroup
-        const bool cols_valid = col0 < args.gn;
+        uint8_t* my_out = sOut + pw * (CPW / 64) * Cfg::BOX_BYTES;
 
-        float acc[128];
+        float acc[CPW];
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < CPW; ++i)
             acc[i] = 0.0f;
 
-        // scalar-mode B scale for chunk c (same for the whole warpgroup)
-        auto load_sb = [&](int c) -> float {
-            if (Cfg::SB_VEC || !cols_valid || c >= nc)
+        // scalar-mode B scale of chunk g (one value per warp), fetched two chunks ahead
+        auto load_sb = [&](int g) -> float {
+            if (Cfg::SB_VEC || g >= my_chunks)
                 return 0.0f;
-            return __ldg(args.sb_scalar + (int64_t)(col0 / 128) * args.sb_col_stride + (int64_t)c * args.sb_chunk_stride);
+            const int tt = g / nc, cc = g - tt * nc;
+            int mm, nn;
+            tile_origin<Cfg>(args, tt, mm, nn);
+            const int col = nn + half * CPW;
+            if (col >= args.gn)
+                return 0.0f;
+            return __ldg(args.sb_scalar + static_cast<int64_t>(col / 128) * args.sb_col_stride +
+                         static_cast<int64_t>(cc) * args.sb_chunk_stride);
         };
-        float sb_next = load_sb(0);
-        bool ok = true;
-        for (int c = 0; c < nc; ++c) {
-            const int s = c % Cfg::STAGES;
-            const uint32_t ph = (c / Cfg::STAGES) & 1;
-            const int b = c & 1;
-            const uint32_t bph = (c >> 1) & 1;
-            const float sb_c = sb_next;
-            sb_next = load_sb(c + 1);
-            if (!mbar_wait(&tfull[b], bph, abort_flag, args.status)) {
-                ok = false;
+        float sb0 = load_sb(0), sb1 = load_sb(1);
+
+        int t = 0, c = 0, m0 = 0, n0 = 0;
+        tile_origin<Cfg>(args, 0, m0, n0);
+        for (int g = 0; g < my_chunks; ++g) {
+            const int s = g % Cfg::STAGES;
+            const uint32_t ph = (g / Cfg::STAGES) & 1;
+            const int b = g & 1;
+            const uint32_t bph = (g >> 1) & 1;
+            const float sb_c = sb0;
+            sb0 = sb1;
+            sb1 = load_sb(g + 2);
+            if (!mbar_wait(&tfull[b], bph, abort_flag, args.status))
                 break;
-            }
             // the scales in stage s landed with full[s]; its phase cannot move on
             // before this warp arrives on empty[s], so this wait returns at once
-            if (!mbar_wait(&full[s], ph, abort_flag, args.status)) {
-                ok = false;
+            if (!mbar_wait(&full[s], ph, abort_flag, args.status))
                 break;
-            }
             tc_fence_after_sync();
             const float sa = sSA[s * Cfg::BM + row];
-            const uint32_t t_base = tmem_base + ((uint32_t)(quarter * 32) << 16) + b * Cfg::BN + g * 128;
+            const float sc = sa * sb_c;
+            const uint32_t t_base =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BN + half * CPW;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_base + j * 32, r);
+            for (int j = 0; j < CPW / 64; ++j) {
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(t_base + j * 64, r0);
+                tmem_ld_32x32b_x32(t_base + j * 64 + 32, r1);
                 tmem_ld_wait();
-                if (j == 3) {
+                if (j == CPW / 64 - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&tempty[b]);
                 }
+                float* a = acc + j * 64;
                 if (Cfg::SB_VEC) {
-                    const float* sbv = sSB + s * Cfg::BN + g * 128 + j * 32;
+                    const float* sbv = sSB + s * Cfg::BN + half * CPW + j * 64;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[j * 32 + i] = fmaf(__uint_as_float(r[i]) * sbv[i], sa, acc[j * 32 + i]);
+                    for (int i = 0; i < 32; ++i) {
+                        a[i] = fmaf(__uint_as_float(r0[i]) * sbv[i], sa, a[i]);
+                        a[32 + i] = fmaf(__uint_as_float(r1[i]) * sbv[32 + i], sa, a[32 + i]);
+                    }
                 } else {
-                    const float sc = sa * sb_c;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[j * 32 + i] = fmaf(__uint_as_float(r[i]), sc, acc[j * 32 + i]);
+                    for (int i = 0; i < 32; ++i) {
+                        a[i] = fmaf(__uint_as_float(r0[i]), sc, a[i]);
+                        a[32 + i] = fmaf(__uint_as_float(r1[i]), sc, a[32 + i]);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[s]);
-        }
-        // all promotion warps take the same decision on whether to write the tile
-        const bool give_up = named_barrier_or(1, 32 * Cfg::PROMO_WARPS, !ok || *abort_flag != 0);
-        if (!give_up) {
-            // BF16 epilogue: two 64-column slabs per warpgroup, 128-byte swizzled
-            uint8_t* stage_base = smem + g * 2 * Cfg::SLAB_BYTES;
+
+            if (++c == nc) {
+                // ------------------------------------------------ BF16 epilogue of tile t
+                const int col0 = n0 + half * CPW;
+                if (lane == 0)
+                    tma_store_wait_read_all();  // this warp's previous stores have left the slab
+                __syncwarp();
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint8_t* slab = stage_base + h * Cfg::SLAB_BYTES;
+                for (int bx = 0; bx < CPW / 64; ++bx) {
+                    uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float* a = acc + h * 64 + k * 8;
-                    uint4 pk;
-                    pk.x = cvt_bf16x2(a[0], a[1]);
-                    pk.y = cvt_bf16x2(a[2], a[3]);
-                    pk.z = cvt_bf16x2(a[4], a[5]);
-                    pk.w = cvt_bf16x2(a[6], a[7]);
-                    *reinterpret_cast<uint4*>(slab + row * 128 + ((k ^ (row & 7)) * 16)) = pk;
+                    for (int k = 0; k < 8; ++k) {
+                        const float* v = acc + bx * 64 + k * 8;
+                        uint4 pk;
+                        pk.x = cvt_bf16x2(v[0], v[1]);
+                        pk.y = cvt_bf16x2(v[2], v[3]);
+                        pk.z = cvt_bf16x2(v[4], v[5]);
+                        pk.w = cvt_bf16x2(v[6], v[7]);
+                        *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                    }
                 }
-            }
-            fence_proxy_async_smem();
-            named_barrier_sync(2 + g, 128);
-            if (quarter == 0 && lane == 0 && cols_valid) {
-                tma_store_2d(&tmD, stage_base, col0, m0);
-                if (col0 + 64 < args.gn)
-                    tma_store_2d(&tmD, stage_base + Cfg::SLAB_BYTES, col0 + 64, m0);
-                tma_store_commit();
-                tma_store_wait_read_all();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int bx = 0; bx < CPW / 64; ++bx)
+                        if (col0 + bx * 64 < args.gn && m0 + quarter * 32 < args.gm)
+                            tma_store_2d(&tmD, my_out + bx * Cfg::BOX_BYTES, col0 + bx * 64, m0 + quarter * 32);
+                    tma_store_commit();
+                }
+#pragma unroll
+                for (int i = 0; i < CPW; ++i)
+                    acc[i] = 0.0f;
+                c = 0;
+                ++t;
+                tile_origin<Cfg>(args, t, m0, n0);
             }
         }
+        if (lane == 0)
+            tma_store_wait_read_all();
     }
 
     tc_fence_before_sync();

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 TILE = 128
 
 
-@pytest.fixture(params=[128], ids=lambda t: f"tileN{t}")
+@pytest.fixture(params=[128, 256], ids=lambda t: f"tileN{t}")
 def tile_n(request):
     prev = bfp8.set_gemm_tile_n(request.param)
     yield request.param
