@@ -169,6 +169,14 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
             cudaSuccess)
             return BFP8_ELAUNCH;
+        // The register split (setmaxnreg) only balances if the kernel was built
+        // with the full per-thread budget; with fewer registers the promotion
+        // warpgroups' setmaxnreg.inc could never be satisfied. Refuse to launch.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        if (Cfg::REG_SPLIT && fa.numRegs < Cfg::LAUNCH_REGS)
+            return BFP8_ELAUNCH;
         attr_set[dev].store(true, std::memory_order_relaxed);
     }
     GemmArgs args;

@@ -76,7 +76,9 @@ struct GemmConfig {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(!REG_SPLIT || 128 * 40 + 256 * 232 <= THREADS * 168, "register split");
+    // registers per thread at launch (65536 / 384, rounded down to a multiple of 8)
+    static constexpr int LAUNCH_REGS = 168;
+    static_assert(!REG_SPLIT || 128 * 40 + 256 * 232 <= THREADS * LAUNCH_REGS, "register split");
 };
 
 struct GemmArgs {
