@@ -41,7 +41,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio on B300 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["mlp", "attn", "stack", "single"], default="mlp")
@@ -264,80 +264,88 @@ def run_ours(args):
     assert bfp8.last_device_status() == 0, "a kernel timed out during warm-up"
 
     # ------------------------------------------------------------ timed region
-    # per-GEMM events around every GEMM launch of the timed steps (same stream)
-    gemm_events = {"fwd": [], "dgrad": [], "wgrad": []}
-    gemm_flops = {"fwd": 0, "dgrad": 0, "wgrad": 0}
+    # One CUDA event between consecutive kernels on the launching stream: the
+    # difference of neighbouring events is that kernel's device time, and the
+    # first and last events bracket the whole timed region.
+    marks = []  # (event, tag, work) of the kernel that ended at this event
+
+    def mark(tag=None, work=0):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        marks.append((e, tag, work))
 
     def timed_step():
         for L, (x, w, dy), lin in zip(layers, inputs, work.linears):
+            M, K, N = lin.M, lin.K, lin.N
             bfp8.fp8_quantize_act(x, L.qx, L.sx)
+            mark("quant_act", quant_bytes(M, K))
             bfp8.fp8_quantize_weight(w, L.qw, L.sw)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+            mark("quant_weight", quant_bytes(N, K))
             bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
-            e1.record(stream)
-            gemm_events["fwd"].append((e0, e1, 2 * lin.M * lin.N * lin.K))
+            mark("gemm_fwd", 2 * M * N * K)
             if fwd_only:
                 continue
             bfp8.fp8_quantize_act(dy, L.qdy, L.sdy)
-            e2 = torch.cuda.Event(enable_timing=True)
-            e3 = torch.cuda.Event(enable_timing=True)
-            e2.record(stream)
+            mark("quant_act", quant_bytes(M, N))
             bfp8.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
-            e3.record(stream)
-            gemm_events["dgrad"].append((e2, e3, 2 * lin.M * lin.N * lin.K))
+            mark("gemm_dgrad", 2 * M * N * K)
             bfp8.fp8_quantize_transpose(dy, L.qdyt, L.sdyt)
+            mark("quant_transpose", quant_bytes(M, N))
             bfp8.fp8_quantize_transpose(x, L.qxt, L.sxt)
-            e4 = torch.cuda.Event(enable_timing=True)
-            e5 = torch.cuda.Event(enable_timing=True)
-            e4.record(stream)
-            bfp8.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, lin.M, L.dw)
-            e5.record(stream)
-            gemm_events["wgrad"].append((e4, e5, 2 * lin.M * lin.N * lin.K))
+            mark("quant_transpose", quant_bytes(M, K))
+            bfp8.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw)
+            mark("gemm_wgrad", 2 * M * N * K)
 
     with ClockSampler(local) as clk:
         barrier(ws)
         torch.cuda.synchronize()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
+        mark()
         for _ in range(args.steps):
             timed_step()
-        t_end.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
     clocks = clk.result()
     status = bfp8.last_device_status()
-    ms_local = t_start.elapsed_time(t_end)
+    ms_local = marks[0][0].elapsed_time(marks[-1][0])
     ms = allreduce_max(ms_local, ws, dev)
     total_flops = work.flops * args.steps * ws
     tflops = total_flops / (ms / 1e3) / 1e12
 
     peaks, peak_src = measured_peaks()
-    fp8_peak_sustained = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    # A kernel timed inside a long step: the sustained (power-capped) figures.
+    fp8_peak = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    hbm_peak = peaks["hbm_gbs"]
     per_kernel = {}
-    for k, evs in gemm_events.items():
-        if not evs:
-            continue
-        t = sum(a.elapsed_time(b) for a, b, _ in evs)
-        fl = sum(f for _, _, f in evs)
-        per_kernel[k] = {"launches": len(evs), "ms_total": round(t, 3), "avg_us": round(1e3 * t / len(evs), 2),
-                         "tflops": round(fl / (t / 1e3) / 1e12, 1), "share_of_step": round(t / ms_local, 4)}
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
-    achieved = per_kernel[dom]["tflops"]
+    for (e0, _, _), (e1, tag, w) in zip(marks[:-1], marks[1:]):
+        k = per_kernel.setdefault(tag, {"launches": 0, "ms": 0.0, "work": 0})
+        k["launches"] += 1
+        k["ms"] += e0.elapsed_time(e1)
+        k["work"] += w
+    kernels = {}
+    for tag, k in per_kernel.items():
+        gemm = tag.startswith("gemm")
+        rate = k["work"] / (k["ms"] / 1e3) / (1e12 if gemm else 1e9)
+        kernels[tag] = {"launches": k["launches"], "ms_total": round(k["ms"], 3),
+                        "avg_us": round(1e3 * k["ms"] / k["launches"], 2),
+                        ("tflops" if gemm else "gbs"): round(rate, 1),
+                        "frac_of_peak": round(rate / (fp8_peak if gemm else hbm_peak), 4),
+                        "share_of_step": round(k["ms"] / ms_local, 4)}
+    dom = max(kernels, key=lambda t: kernels[t]["ms_total"])
+    gemm_dom = dom.startswith("gemm")
+    achieved = kernels[dom]["tflops" if gemm_dom else "gbs"]
     traffic = None
-    tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
-            tr = json.load(f)
-        if tr.get("workload") == work.name and tr.get("kernel") == dom and tr.get("source_sha") == _gemm_sha():
+            tr = json.load(f).get(dom, {})
+        if tr.get("workload") == work.name and tr.get("source_sha") == _kernel_sha():
             traffic = tr.get("dram_bytes_per_launch")
-    roofline = {"bound": "tensor", "kernel": f"bfp8_gemm_kernel ({dom})", "achieved": achieved,
-                "peak": round(fp8_peak_sustained, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp8_peak_sustained, 4), "traffic": traffic,
-                "peak_source": (f"{peak_src}: 2 x bf16_tflops_sustained ({peaks['bf16_tflops_sustained']}) "
-                                f"from MEASURED_PEAKS.json, FP8/BF16 nominal ratio 2")}
+    roofline = {"bound": "tensor" if gemm_dom else "hbm", "kernel": dom, "achieved": achieved,
+                "peak": round(fp8_peak if gemm_dom else hbm_peak, 1), "unit": "TFLOP/s" if gemm_dom else "GB/s",
+                "frac": round(kernels[dom]["frac_of_peak"], 4), "traffic": traffic,
+                "peak_source": (f"{peak_src}: 2 x bf16_tflops_sustained ({peaks['bf16_tflops_sustained']}), "
+                                f"FP8/BF16 nominal dense ratio 2" if gemm_dom else
+                                f"{peak_src}: hbm_gbs ({hbm_peak})")}
 
     # ------------------------------------------------------------ end to end (host buffers)
     e2e = None
@@ -386,12 +394,12 @@ def run_ours(args):
             "metric": METRIC, "value": round(tflops, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-            "pct_of_fp8_peak": round(100 * tflops / fp8_peak_sustained, 2),
+            "pct_of_fp8_peak": round(100 * tflops / fp8_peak, 2),
             "config": {"workload": work.name, "linears": [f"{l.name}: M={l.M} K={l.K} N={l.N} x~{l.x_dist}"
                                                           for l in work.linears],
                        "passes": "+".join(work.passes) + " incl. all quantisers",
                        "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (no flush)"},
-            "roofline": roofline, "kernels": per_kernel, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": kernels_per_step * args.steps, "clocks": clocks,
             "device_status": bfp8.STATUS.get(status, status),
         }
@@ -401,10 +409,16 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _gemm_sha():
+def quant_bytes(R: int, C: int) -> int:
+    """Algorithmic HBM bytes of one quantiser call on an R x C tensor: BF16 read, code write, FP32 scales."""
+    return 2 * R * C + R * C + 4 * R * (C // 128)
+
+
+def _kernel_sha():
+    """Hash of the kernel sources: a stored ncu traffic figure is only used while it still matches."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh"):
+    for f in ("gemm.cuh", "ptx.cuh", "quant.cuh", "bfp8.cu"):
         with open(os.path.join(ROOT, "blockwise_fp8_linear_weight_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
