@@ -1,8 +1,9 @@
 """Benchmark of the blockwise-FP8 linear layer on B300: fwd + dgrad + wgrad at Puro-2B shapes.
 
-One step = the whole hot path for every linear of the workload: quantise x
-(1x128), quantise W (128x128), forward GEMM; quantise dy, input-gradient GEMM;
-quantise dy and x transposed, weight-gradient GEMM (8 kernels per linear).
+One step = the whole hot path for every linear of the workload: quantise x in
+both layouts (1x128 along K, and along M transposed), quantise W (128x128),
+forward GEMM; quantise dy in both layouts, input-gradient GEMM, weight-gradient
+GEMM (6 kernels per linear).
 The metric is TFLOPS of the three GEMMs (3 x 2MNK per linear) over the whole
 step time, quantisers included.
 
@@ -85,6 +86,12 @@ def allreduce_max(v: float, ws: int, device=None) -> float:
     t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(flops_per_step: int, steps: int, ws: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of the same workload (replicas, weak
+    scaling), so the job's work is ws x steps x flops_per_step over the slowest rank's time."""
+    return flops_per_step * steps * ws / (ms_max / 1e3) / 1e12
 
 
 def barrier(ws: int):
@@ -252,11 +259,15 @@ def run_ours(args):
 
     def step():
         for L, (x, w, dy) in zip(layers, inputs):
-            L.forward(x, w)
-            if not fwd_only:
+            if fwd_only:
+                bfp8.fp8_quantize_act(x, L.qx, L.sx)
+                bfp8.fp8_quantize_weight(w, L.qw, L.sw)
+                bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+            else:
+                L.forward(x, w)
                 L.backward(dy)
 
-    kernels_per_step = sum(3 if fwd_only else 8 for _ in layers)
+    kernels_per_step = sum(3 if fwd_only else L.KERNELS_PER_STEP for L in layers)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step()
@@ -277,22 +288,22 @@ def run_ours(args):
     def timed_step():
         for L, (x, w, dy), lin in zip(layers, inputs, work.linears):
             M, K, N = lin.M, lin.K, lin.N
-            bfp8.fp8_quantize_act(x, L.qx, L.sx)
-            mark("quant_act", quant_bytes(M, K))
+            if fwd_only:
+                bfp8.fp8_quantize_act(x, L.qx, L.sx)
+                mark("quant_act", quant_bytes(M, K))
+            else:
+                bfp8.fp8_quantize_act_transpose(x, L.qx, L.sx, L.qxt, L.sxt)
+                mark("quant_act_transpose", dual_bytes(M, K))
             bfp8.fp8_quantize_weight(w, L.qw, L.sw)
             mark("quant_weight", quant_bytes(N, K))
             bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
             mark("gemm_fwd", 2 * M * N * K)
             if fwd_only:
                 continue
-            bfp8.fp8_quantize_act(dy, L.qdy, L.sdy)
-            mark("quant_act", quant_bytes(M, N))
+            bfp8.fp8_quantize_act_transpose(dy, L.qdy, L.sdy, L.qdyt, L.sdyt)
+            mark("quant_act_transpose", dual_bytes(M, N))
             bfp8.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
             mark("gemm_dgrad", 2 * M * N * K)
-            bfp8.fp8_quantize_transpose(dy, L.qdyt, L.sdyt)
-            mark("quant_transpose", quant_bytes(M, N))
-            bfp8.fp8_quantize_transpose(x, L.qxt, L.sxt)
-            mark("quant_transpose", quant_bytes(M, K))
             bfp8.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw)
             mark("gemm_wgrad", 2 * M * N * K)
 
@@ -308,8 +319,7 @@ def run_ours(args):
     status = bfp8.last_device_status()
     ms_local = marks[0][0].elapsed_time(marks[-1][0])
     ms = allreduce_max(ms_local, ws, dev)
-    total_flops = work.flops * args.steps * ws
-    tflops = total_flops / (ms / 1e3) / 1e12
+    tflops = job_tflops(work.flops, args.steps, ws, ms)
 
     peaks, peak_src = measured_peaks()
     # A kernel timed inside a long step: the sustained (power-capped) figures.
@@ -361,7 +371,12 @@ def run_ours(args):
             for L, h, d, o in zip(layers, host, dev_in, outs_host):
                 for src, dst in zip(h, d):
                     dst.copy_(src, non_blocking=True)
-                L.forward(d[0], d[1])
+                if fwd_only:
+                    bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
+                    bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
+                    bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+                else:
+                    L.forward(d[0], d[1])
                 o[0].copy_(L.y, non_blocking=True)
                 if not fwd_only:
                     L.backward(d[2])
@@ -407,6 +422,12 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def dual_bytes(R: int, C: int) -> int:
+    """Algorithmic HBM bytes of one two-layout quantiser call: one BF16 read, two code layouts, two scale sets."""
+    r128 = (R + 127) // 128 * 128
+    return 2 * R * C + R * C + C * r128 + 4 * R * (C // 128) + 4 * C * (r128 // 128)
 
 
 def quant_bytes(R: int, C: int) -> int:

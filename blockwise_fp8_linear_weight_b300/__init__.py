@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   fp8_quantize_act(x)            -> (q [R,C] u8, s [C/128, R] f32)
   fp8_quantize_weight(w)         -> (q [N,K] u8, s [N/128, K/128] f32)
   fp8_quantize_transpose(x)      -> (qt [C, R128] u8, st [R128/128, C] f32)
+  fp8_quantize_act_transpose(x)  -> (q, s, qt, st): both layouts, one read of x
   fp8_block_gemm_fwd(qx, sx, qw, sw)        -> y  [M, N] bf16
   fp8_block_gemm_dgrad(qdy, sdy, qw, sw)    -> dx [M, K] bf16
   fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M) -> dw [N, K] bf16
@@ -58,6 +59,7 @@ def load_library(path: str = LIB_PATH):
         "fp8_quantize_act": [p, i64, i64, i64, p, i64, p, i64, p],
         "fp8_quantize_weight": [p, i64, i64, i64, p, i64, p, p],
         "fp8_quantize_transpose": [p, i64, i64, i64, p, i64, p, i64, p],
+        "fp8_quantize_act_transpose": [p, i64, i64, i64, p, i64, p, i64, p, i64, p, i64, p],
         "fp8_block_gemm_fwd": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
         "fp8_block_gemm_dgrad": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
         "fp8_block_gemm_wgrad": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
@@ -156,6 +158,24 @@ def fp8_quantize_transpose(x, qt=None, st=None):
     return qt, st
 
 
+def fp8_quantize_act_transpose(x, q=None, s=None, qt=None, st=None):
+    """Both layouts of x [R, C] (bf16) in one pass: (q, s) as fp8_quantize_act, (qt, st) as
+    fp8_quantize_transpose."""
+    lib = load_library()
+    _req(x, torch.bfloat16, "x")
+    R, C = x.shape
+    R128 = _round_up(R, TILE)
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device) if q is None else q
+    s = _scales(C // TILE if C % TILE == 0 else 0, R, x.device) if s is None else s
+    qt = torch.empty((C, R128), dtype=torch.uint8, device=x.device) if qt is None else qt
+    if st is None:
+        st = torch.empty((R128 // TILE, _round_up(C, 4)), dtype=torch.float32, device=x.device)[:, :C]
+    _check("fp8_quantize_act_transpose", lib.fp8_quantize_act_transpose(
+        _ptr(x), R, C, x.stride(0), _ptr(q), q.stride(0), _ptr(s), s.stride(0),
+        _ptr(qt), qt.stride(0), _ptr(st), st.stride(0), _stream()))
+    return q, s, qt, st
+
+
 # ----------------------------------------------------------------------- GEMMs
 def fp8_block_gemm_fwd(qx, sx, qw, sw, y=None):
     """y [M, N] bf16 = blockwise-FP8 x W^T from (qx [M,K], sx [K/128, M], qw [N,K], sw [N/128, K/128])."""
@@ -210,12 +230,15 @@ def set_gemm_tile_n(tile_n: int) -> int:
 class BlockwiseFP8Linear:
     """Buffers and call sequence of one blockwise-FP8 linear layer y = x W^T (x [M,K], W [N,K]).
 
-    ``forward(x, w)`` quantises x (1x128) and W (128x128) and runs the forward
-    GEMM; ``backward(dy)`` quantises dy (1x128 along N, and transposed along M),
-    quantises x transposed, and runs the input- and weight-gradient GEMMs. All
-    outputs live in buffers allocated once, so a training step launches exactly
-    eight kernels and allocates nothing.
+    ``forward(x, w)`` quantises x in both layouts (1x128 along K for the
+    forward GEMM, 1x128 along M, transposed, for the weight-gradient GEMM) and
+    W (128x128), then runs the forward GEMM; ``backward(dy)`` quantises dy in
+    both layouts and runs the input- and weight-gradient GEMMs. All outputs
+    live in buffers allocated once, so a training step launches exactly six
+    kernels and allocates nothing.
     """
+
+    KERNELS_PER_STEP = 6
 
     def __init__(self, M: int, K: int, N: int, device="cuda"):
         self.M, self.K, self.N = M, K, N
@@ -235,21 +258,15 @@ class BlockwiseFP8Linear:
         self.y = torch.empty((M, N), dtype=bf, device=dev)
         self.dx = torch.empty((M, K), dtype=bf, device=dev)
         self.dw = torch.empty((N, K), dtype=bf, device=dev)
-        self._x = None
 
     def forward(self, x, w):
-        fp8_quantize_act(x, self.qx, self.sx)
+        fp8_quantize_act_transpose(x, self.qx, self.sx, self.qxt, self.sxt)
         fp8_quantize_weight(w, self.qw, self.sw)
         fp8_block_gemm_fwd(self.qx, self.sx, self.qw, self.sw, self.y)
-        self._x = x
         return self.y
 
     def backward(self, dy):
-        fp8_quantize_act(dy, self.qdy, self.sdy)
+        fp8_quantize_act_transpose(dy, self.qdy, self.sdy, self.qdyt, self.sdyt)
         fp8_block_gemm_dgrad(self.qdy, self.sdy, self.qw, self.sw, self.dx)
-        fp8_quantize_transpose(dy, self.qdyt, self.sdyt)
-        fp8_quantize_transpose(self._x, self.qxt, self.sxt)
         fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw)
         return self.dx, self.dw
-
-    KERNELS_PER_STEP = 8

@@ -246,7 +246,7 @@ extern "C" int fp8_quantize_act(const void* x, int64_t R, int64_t C, int64_t ldx
         return rc;
     const int64_t nchunks = C / 128;
     const int64_t ntiles = R * nchunks;
-    constexpr int UNROLL = 2;
+    constexpr int UNROLL = 4;
     const int64_t blocks = (ntiles + 16 * UNROLL - 1) / (16 * UNROLL);
     quant_act_kernel<UNROLL><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), ldx, q, ldq, s, lds, nchunks, ntiles);
@@ -295,6 +295,31 @@ extern "C" int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64
     dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R128 / 128));
     quant_transpose_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), R, ldx, qt, ldqt, st, ldst);
+    return launch_status();
+}
+
+extern "C" int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                                          int64_t ldq, float* s, int64_t lds, uint8_t* qt, int64_t ldqt,
+                                          float* st, int64_t ldst, void* stream)
+{
+    if (R < 0 || C < 0)
+        return BFP8_EINVAL;
+    if (C % 128 || R > kMaxDim || C > kMaxDim || (R + 127) / 128 > kMaxGridY)
+        return BFP8_ESHAPE;
+    if (R == 0 || C == 0)
+        return BFP8_OK;
+    const int64_t R128 = (R + 127) / 128 * 128;
+    if (!x || !q || !s || !qt || !st || ldx < C || ldq < C || lds < R || ldqt < R128 || ldst < C)
+        return BFP8_EINVAL;
+    if (!aligned(x, 16) || ldx % 8 || !aligned(q, 8) || ldq % 8 || !aligned(s, 4) || !aligned(qt, 16) ||
+        ldqt % 16 || !aligned(st, 8) || ldst % 2)
+        return BFP8_EALIGN;
+    int rc = check_arch(nullptr);
+    if (rc != BFP8_OK)
+        return rc;
+    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R128 / 128));
+    quant_dual_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), R, ldx, q, ldq, s, lds, qt, ldqt, st, ldst);
     return launch_status();
 }
 

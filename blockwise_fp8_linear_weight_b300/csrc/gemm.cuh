@@ -14,21 +14,25 @@
 //
 // Persistent kernel, one CTA per SM, output tiles of 128 x BN visited in a
 // static round-robin order (the smaller operand is re-read from L2, the larger
-// one streamed once). Warp roles:
-//   warp 0      TMA producer: per chunk the A tile 128x128, the B tile (BNx128
-//               K-major, or 128-column boxes of an MN-major operand), the A
-//               scales and, in vector mode, the B scales, into a STAGES-deep
-//               shared-memory ring;
+// one streamed once). Two shared-memory rings:
+//   operand ring (STAGES deep): the A tile 128x128 and the B tile (BNx128
+//     K-major, or 128-column boxes of an MN-major operand) of one chunk; a
+//     stage is handed back to the producer by the MMA completion alone;
+//   scale ring (SSTAGES deep): the chunk's 128 A scales and, in vector mode,
+//     its BN B scales; a stage is handed back by the promotion warps.
+// Warp roles:
+//   warp 0      TMA producer of both rings;
 //   warp 1      allocates TMEM; one thread issues 4 tcgen05.mma (K = 32 each)
 //               per chunk into one of two TMEM accumulators of BN columns;
 //   warps 4..11 promotion: warp w owns TMEM lanes 32 (w%4) .. +31 (output rows)
 //               and BN/2 columns; per chunk it reads the partial sums with
 //               tcgen05.ld (two loads in flight per wait), releases the TMEM
 //               buffer and accumulates  acc += partial * (sA * sB)  in FP32
-//               registers; after the last chunk of a tile it rounds acc
-//               to BF16, stages it in its own 128-byte-swizzled shared-memory
-//               slab and issues TMA stores (the TMA unit drops rows and columns
-//               outside D), overlapping the MMAs of the next tile.
+//               registers; after the last chunk of a
+//               tile it rounds acc to BF16, stages it in its own 128-byte-
+//               swizzled shared-memory slab and issues TMA stores (the TMA unit
+//               drops rows and columns outside D), overlapping the MMAs of the
+//               next tile.
 // With BN = 256 the promotion warps need more than the 168 registers a
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
 // warpgroup (40 each) to the promotion warpgroups (232 each):
@@ -41,6 +45,13 @@
 
 #include "ptx.cuh"
 
+// Promotion arithmetic: 1 = packed two-lane FP32 instructions, 0 = scalar FMA.
+// The packed form issues half the instructions but the FP32 pipe processes the
+// same number of lanes per clock, so it is off by default.
+#ifndef BFP8_PROMO_F32X2
+#define BFP8_PROMO_F32X2 0
+#endif
+
 namespace bfp8 {
 
 template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_>
@@ -49,6 +60,7 @@ struct GemmConfig {
     static constexpr int BN = BN_;
     static constexpr int BK = 128;
     static constexpr int STAGES = STAGES_;
+    static constexpr int SSTAGES = 8;
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
     static constexpr int PROMO_WARPS = 8;
@@ -60,7 +72,8 @@ struct GemmConfig {
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SA_BYTES = BM * 4;
     static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;
-    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + SA_BYTES + SB_BYTES;
+    static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
+    static constexpr uint32_t SC_TX = SA_BYTES + SB_BYTES;
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 64 bf16 (4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
     static constexpr int STAGE_OUT_BYTES = PROMO_WARPS * (CPW / 64) * BOX_BYTES;
@@ -69,9 +82,9 @@ struct GemmConfig {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_OUT = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SA = OFF_OUT + STAGE_OUT_BYTES;
-    static constexpr int OFF_SB = OFF_SA + STAGES * SA_BYTES;
-    static constexpr int OFF_BAR = OFF_SB + STAGES * SB_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
+    static constexpr int OFF_SB = OFF_SA + SSTAGES * SA_BYTES;
+    static constexpr int OFF_BAR = OFF_SB + SSTAGES * SB_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * SSTAGES + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
@@ -120,10 +133,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     float* sSA = reinterpret_cast<float*>(smem + Cfg::OFF_SA);
     float* sSB = reinterpret_cast<float*>(smem + Cfg::OFF_SB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + Cfg::STAGES;
-    uint64_t* tfull = bars + 2 * Cfg::STAGES;
-    uint64_t* tempty = tfull + 2;
+    uint64_t* full = bars;                       // operand stage landed (TMA)
+    uint64_t* empty = full + Cfg::STAGES;        // operand stage consumed (MMA commit)
+    uint64_t* sfull = empty + Cfg::STAGES;       // scale stage landed (TMA)
+    uint64_t* sempty = sfull + Cfg::SSTAGES;     // scale stage consumed (promotion warps)
+    uint64_t* tfull = sempty + Cfg::SSTAGES;     // TMEM buffer holds a finished chunk
+    uint64_t* tempty = tfull + 2;                // TMEM buffer read out
     uint64_t* mma_done = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
@@ -140,7 +155,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + Cfg::PROMO_WARPS);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < Cfg::SSTAGES; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sempty[s], Cfg::PROMO_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
@@ -183,7 +202,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t ph = (g / Cfg::STAGES) & 1;
                 if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status))
                     break;
-                mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                mbar_arrive_expect_tx(&full[s], Cfg::OP_TX);
                 tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], c * Cfg::BK, m0);
                 if (Cfg::B_MN) {
 #pragma unroll
@@ -193,9 +212,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     tma_load_2d(sB + s * Cfg::B_BYTES, &tmB, &full[s], c * Cfg::BK, n0);
                 }
-                tma_load_2d(sSA + s * Cfg::BM, &tmSA, &full[s], m0, c);
+                const int ss = g % Cfg::SSTAGES;
+                const uint32_t sph = (g / Cfg::SSTAGES) & 1;
+                if (!mbar_wait(&sempty[ss], sph ^ 1, abort_flag, args.status)) {
+                    ++issued;  // the operand copies of chunk g are in flight
+                    break;
+                }
+                mbar_arrive_expect_tx(&sfull[ss], Cfg::SC_TX);
+                tma_load_2d(sSA + ss * Cfg::BM, &tmSA, &sfull[ss], m0, c);
                 if (Cfg::SB_VEC)
-                    tma_load_2d(sSB + s * Cfg::BN, &tmSB, &full[s], n0, c);
+                    tma_load_2d(sSB + ss * Cfg::BN, &tmSB, &sfull[ss], n0, c);
                 ++issued;
                 if (++c == nc) {
                     c = 0;
@@ -203,10 +229,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tile_origin<Cfg>(args, t, m0, n0);
                 }
             }
-            // make sure no copy is still landing in shared memory before exit
-            for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g) {
-                volatile int never = 0;
+            // make sure no copy is still landing in shared memory before exit: wait
+            // for the last phase of every stage that was filled
+            volatile int never = 0;
+            for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g)
                 mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status);
+            const int sissued = issued;  // scale copies issued (the last one may be missing on abort)
+            for (int g = sissued - Cfg::SSTAGES < 0 ? 0 : sissued - Cfg::SSTAGES; g < sissued; ++g) {
+                // an abort between the operand and the scale copy of chunk g leaves sfull
+                // without that phase; its wait then ends at the time limit
+                mbar_wait(&sfull[g % Cfg::SSTAGES], (g / Cfg::SSTAGES) & 1, &never, args.status);
             }
         }
     } else if (warp == 1) {
@@ -277,21 +309,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int t = 0, c = 0, m0 = 0, n0 = 0;
         tile_origin<Cfg>(args, 0, m0, n0);
         for (int g = 0; g < my_chunks; ++g) {
-            const int s = g % Cfg::STAGES;
-            const uint32_t ph = (g / Cfg::STAGES) & 1;
+            const int ss = g % Cfg::SSTAGES;
+            const uint32_t sph = (g / Cfg::SSTAGES) & 1;
             const int b = g & 1;
             const uint32_t bph = (g >> 1) & 1;
             const float sb_c = sb0;
             sb0 = sb1;
             sb1 = load_sb(g + 2);
+            if (!mbar_wait(&sfull[ss], sph, abort_flag, args.status))
+                break;
             if (!mbar_wait(&tfull[b], bph, abort_flag, args.status))
                 break;
-            // the scales in stage s landed with full[s]; its phase cannot move on
-            // before this warp arrives on empty[s], so this wait returns at once
-            if (!mbar_wait(&full[s], ph, abort_flag, args.status))
-                break;
             tc_fence_after_sync();
-            const float sa = sSA[s * Cfg::BM + row];
+            const float sa = sSA[ss * Cfg::BM + row];
             const float sc = sa * sb_c;
             const uint32_t t_base =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BN + half * CPW;
@@ -309,23 +339,60 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 float* a = acc + j * 64;
                 if (Cfg::SB_VEC) {
-                    const float* sbv = sSB + s * Cfg::BN + half * CPW + j * 64;
+                    // per-column scales: broadcast 16-byte shared-memory reads
+                    const float4* sbv = reinterpret_cast<const float4*>(sSB + ss * Cfg::BN + half * CPW + j * 64);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        a[i] = fmaf(__uint_as_float(r0[i]) * sbv[i], sa, a[i]);
-                        a[32 + i] = fmaf(__uint_as_float(r1[i]) * sbv[32 + i], sa, a[32 + i]);
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 v0 = sbv[i];
+                        const float4 v1 = sbv[8 + i];
+                        float p[8];
+#if BFP8_PROMO_F32X2
+                        fmul2(p[0], p[1], __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]), v0.x, v0.y);
+                        fmul2(p[2], p[3], __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]), v0.z, v0.w);
+                        fmul2(p[4], p[5], __uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), v1.x, v1.y);
+                        fmul2(p[6], p[7], __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]), v1.z, v1.w);
+                        ffma2(a[4 * i], a[4 * i + 1], p[0], p[1], sa, sa);
+                        ffma2(a[4 * i + 2], a[4 * i + 3], p[2], p[3], sa, sa);
+                        ffma2(a[32 + 4 * i], a[32 + 4 * i + 1], p[4], p[5], sa, sa);
+                        ffma2(a[32 + 4 * i + 2], a[32 + 4 * i + 3], p[6], p[7], sa, sa);
+#else
+                        p[0] = __uint_as_float(r0[4 * i]) * v0.x;
+                        p[1] = __uint_as_float(r0[4 * i + 1]) * v0.y;
+                        p[2] = __uint_as_float(r0[4 * i + 2]) * v0.z;
+                        p[3] = __uint_as_float(r0[4 * i + 3]) * v0.w;
+                        p[4] = __uint_as_float(r1[4 * i]) * v1.x;
+                        p[5] = __uint_as_float(r1[4 * i + 1]) * v1.y;
+                        p[6] = __uint_as_float(r1[4 * i + 2]) * v1.z;
+                        p[7] = __uint_as_float(r1[4 * i + 3]) * v1.w;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            a[4 * i + k] = fmaf(p[k], sa, a[4 * i + k]);
+                            a[32 + 4 * i + k] = fmaf(p[4 + k], sa, a[32 + 4 * i + k]);
+                        }
+#endif
                     }
                 } else {
+#if BFP8_PROMO_F32X2
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        ffma2(a[2 * i], a[2 * i + 1], __uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
+                              sc, sc);
+                        ffma2(a[32 + 2 * i], a[32 + 2 * i + 1], __uint_as_float(r1[2 * i]),
+                              __uint_as_float(r1[2 * i + 1]), sc, sc);
+                    }
+#else
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         a[i] = fmaf(__uint_as_float(r0[i]), sc, a[i]);
                         a[32 + i] = fmaf(__uint_as_float(r1[i]), sc, a[32 + i]);
                     }
+#endif
                 }
             }
+            // this warp is done with the chunk's scales
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&empty[s]);
+                mbar_arrive(&sempty[ss]);
 
             if (++c == nc) {
                 // ------------------------------------------------ BF16 epilogue of tile t

@@ -6,12 +6,29 @@
 // convention implemented here: activation tiles of 1x128 along the contraction
 // axis, weight blocks of 128x128, scale s = fl32(amax / 448), code =
 // e4m3_rn_satfinite(fl32(x / s)); an all-zero tile gets s = 0 and signed-zero
-// codes. Both divisions are IEEE binary32 divisions (__fdiv_rn), so codes and
-// scales are reproducible bit for bit.
+// codes. Both divisions are IEEE binary32 divisions, so codes and scales are
+// reproducible bit for bit.
 //
-// All three kernels are HBM-bound (2 B read + 1 B written per element): reads
-// are 16-byte vector loads that cover whole 128-byte lines, amax reductions
-// use warp shuffles (or a shared-memory column pass in the transposed kernel).
+// Exact codes without a division per element. Let r = fl32(1/s) and
+// t = fl32(x * r). Each of the two roundings is off by a relative 2^-24 at
+// most, so t is within 2 units in the last place (ulp) of the exact quotient
+// x/s, and within 3 ulp of fl32(x/s). The E4M3 code of a binary32 value only
+// changes where the value crosses a rounding boundary of the E4M3 grid: in the
+// normal E4M3 range (|t| >= 2^-6) those boundaries are the binary32 numbers
+// whose low 20 mantissa bits are 0x80000 (the midpoint between two codes with
+// 3 mantissa bits). If t's low 20 bits are more than 4 units away from that
+// pattern, t and fl32(x/s) lie on the same side of every boundary and encode to
+// the same code. Below 2^-11 both encode to a signed zero (the smallest
+// non-zero code is 2^-9, so the boundary is 2^-10). Everything else - values
+// within 4 ulp of a boundary, the subnormal E4M3 range [2^-11, 2^-6), and tiles
+// whose scale is a binary32 subnormal (1/s may then overflow) - takes the IEEE
+// division. The slow path is rare (about one element in 10^4 for normal data)
+// and only changes which instructions compute fl32(x/s), never the result.
+//
+// All four kernels are HBM-bound (2 B read + 1 B written per element and per
+// code layout): reads are 16-byte vector loads that cover whole 128-byte lines,
+// amax reductions use warp shuffles (or a shared-memory column pass for the
+// transposed layout).
 #pragma once
 
 #include <cstdint>
@@ -20,20 +37,62 @@
 
 namespace bfp8 {
 
-// Scale of a tile from its amax; 0 for an all-zero tile.
-__device__ __forceinline__ float tile_scale(float amax)
+// A tile's scale and, when usable, its reciprocal.
+struct TileScale {
+    float s;   // fl32(amax / 448), 0 for an all-zero tile
+    float r;   // fl32(1 / s) if s is a normal binary32 number
+    bool fast; // r is usable
+};
+
+__device__ __forceinline__ TileScale tile_scale(float amax)
 {
-    return __fdiv_rn(amax, 448.0f);
+    TileScale t;
+    t.s = __fdiv_rn(amax, 448.0f);
+    t.fast = t.s >= 1.17549435e-38f;  // smallest normal binary32
+    t.r = t.fast ? __frcp_rn(t.s) : 0.0f;
+    return t;
 }
 
-// Codes of two BF16 values (packed in one word) under scale s.
-__device__ __forceinline__ uint32_t codes2(uint32_t w, float s)
+// True if the E4M3 code of t equals that of fl32(x / s) (see the header comment).
+__device__ __forceinline__ bool quotient_safe(float t)
 {
-    if (s == 0.0f) {
-        // signed zeros: the sign bits of the two inputs
-        return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+    const uint32_t u = __float_as_uint(t) & 0x7FFFFFFFu;
+    const bool tiny = u < 0x3A000000u;                            // |t| < 2^-11: code +-0
+    const bool normal = u >= 0x3C800000u;                         // |t| >= 2^-6
+    const bool far = ((u & 0xFFFFFu) - 0x7FFFCu) > 8u;            // not within 4 ulp of a midpoint
+    return tiny || (normal && far);
+}
+
+// fl32(x / s), the definition's quotient, by the exact route. Kept out of line
+// so that the compiler cannot evaluate the division speculatively on the
+// fast path; it only runs for the rare values that need it.
+__device__ __noinline__ float exact_quotient(float x, float s, float t, bool fast)
+{
+    if (fast && quotient_safe(t))
+        return t;
+    // all-zero tile: every x is +-0 and its code is the signed zero itself
+    return s == 0.0f ? x : __fdiv_rn(x, s);
+}
+
+// Codes of N values (N even); out[i] packs codes 4i .. 4i+3, first value in the low byte.
+template <int N>
+__device__ __forceinline__ void encode(const float (&x)[N], const TileScale& ts, uint32_t (&out)[N / 4])
+{
+    float t[N];
+    bool ok = ts.fast;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        t[i] = x[i] * ts.r;
+        ok = ok & quotient_safe(t[i]);
     }
-    return cvt_e4m3x2(__fdiv_rn(bf16_lo(w), s), __fdiv_rn(bf16_hi(w), s));
+    if (!ok) {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            t[i] = exact_quotient(x[i], ts.s, t[i], ts.fast);
+    }
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i)
+        out[i] = cvt_e4m3x2(t[4 * i], t[4 * i + 1]) | (cvt_e4m3x2(t[4 * i + 2], t[4 * i + 3]) << 16);
 }
 
 __device__ __forceinline__ float amax_word(uint32_t w)
@@ -47,19 +106,30 @@ __device__ __forceinline__ float amax_v4(const uint4& v)
 }
 
 // 8 BF16 values -> 8 codes (one 64-bit word, first value in the low byte).
-__device__ __forceinline__ uint2 codes8(const uint4& v, float s)
+__device__ __forceinline__ uint2 codes8(const uint4& v, const TileScale& ts)
 {
-    uint2 o;
-    o.x = codes2(v.x, s) | (codes2(v.y, s) << 16);
-    o.y = codes2(v.z, s) | (codes2(v.w, s) << 16);
-    return o;
+    const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    uint32_t o[2];
+    encode<8>(x, ts, o);
+    return make_uint2(o[0], o[1]);
+}
+
+// amax over the 16 lanes that share one 1x128 tile (lanes 0-15 or 16-31).
+__device__ __forceinline__ float amax16(float a)
+{
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    return a;
 }
 
 // ---------------------------------------------------------------------------
 // 1x128 activation tiles along the columns of x [R][C] (C a multiple of 128).
 // 16 threads own one tile (8 values each); a warp covers two neighbouring
 // tiles, i.e. 512 contiguous bytes of a row. Each thread handles UNROLL tiles
-// (loads issued first for memory-level parallelism).
+// (all loads issued first for memory-level parallelism).
 // q [R][C] (ldq), s [C/128][R] (lds).
 // ---------------------------------------------------------------------------
 template <int UNROLL>
@@ -83,18 +153,14 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restri
     }
 #pragma unroll
     for (int u = 0; u < UNROLL; ++u) {
-        float a = amax_v4(v[u]);
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        const float a = amax16(amax_v4(v[u]));
         const int64_t t = first + u * 16;
         if (t < ntiles) {
             const int64_t r = t / nchunks, c = t - r * nchunks;
-            const float sc = tile_scale(a);
-            *reinterpret_cast<uint2*>(q + r * ldq + c * 128 + sub * 8) = codes8(v[u], sc);
+            const TileScale ts = tile_scale(a);
+            *reinterpret_cast<uint2*>(q + r * ldq + c * 128 + sub * 8) = codes8(v[u], ts);
             if (sub == 0)
-                s[c * lds + r] = sc;
+                s[c * lds + r] = ts.s;
         }
     }
 }
@@ -132,13 +198,76 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
 #pragma unroll
     for (int i = 1; i < 8; ++i)
         a = fmaxf(a, red[i]);
-    const float sc = tile_scale(a);
+    const TileScale ts = tile_scale(a);
     uint8_t* qb = q + (bi * 128 + r0) * ldq + bj * 128 + cg * 8;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<uint2*>(qb + (int64_t)(16 * i) * ldq) = codes8(v[i], sc);
+        *reinterpret_cast<uint2*>(qb + (int64_t)(16 * i) * ldq) = codes8(v[i], ts);
     if (tid == 0)
-        s[bi * kblocks + bj] = sc;
+        s[bi * kblocks + bj] = ts.s;
+}
+
+// ---------------------------------------------------------------------------
+// Column pass shared by the transposed and the dual kernel. The 128x128 BF16
+// block sits row-major in shared memory (rows past R hold +0). Warp w takes
+// rows 32 (w%4) .. +31 of the column pair 64 (w/4) + 2 lane, +1 (conflict-free
+// 4-byte reads); the four row quarters combine their amax through shared
+// memory. Codes go to qt [C][R128] (row = input column), scales to
+// st [R128/128][C]. Pad rows hold +0 and so get code 0x00.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], float (*part)[128], int64_t cb, int64_t rb,
+                                            uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ st,
+                                            int64_t ldst)
+{
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;
+    const int col = (warp >> 2) * 64 + 2 * lane;  // first of the thread's two columns
+    float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t w = tile[quarter * 32 + i][col >> 1];
+        a0 = fmaxf(a0, fabsf(bf16_lo(w)));
+        a1 = fmaxf(a1, fabsf(bf16_hi(w)));
+    }
+    *reinterpret_cast<float2*>(&part[quarter][col]) = make_float2(a0, a1);
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const float2 p = *reinterpret_cast<const float2*>(&part[qq][col]);
+        a0 = fmaxf(a0, p.x);
+        a1 = fmaxf(a1, p.y);
+    }
+    const TileScale s0 = tile_scale(a0), s1 = tile_scale(a1);
+
+    // column col: low halves; column col+1: high halves. 32 rows -> 32 codes each,
+    // re-read from shared memory and encoded 8 at a time to bound register use.
+    uint32_t c0[8], c1[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x0[8], x1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = tile[quarter * 32 + 8 * j + i][col >> 1];
+            x0[i] = bf16_lo(w);
+            x1[i] = bf16_hi(w);
+        }
+        uint32_t o0[2], o1[2];
+        encode<8>(x0, s0, o0);
+        encode<8>(x1, s1, o1);
+        c0[2 * j] = o0[0];
+        c0[2 * j + 1] = o0[1];
+        c1[2 * j] = o1[0];
+        c1[2 * j + 1] = o1[1];
+    }
+    uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + quarter * 32;
+    uint8_t* out1 = out0 + ldqt;
+    reinterpret_cast<uint4*>(out0)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+    reinterpret_cast<uint4*>(out0)[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
+    reinterpret_cast<uint4*>(out1)[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+    reinterpret_cast<uint4*>(out1)[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+    if (quarter == 0)
+        *reinterpret_cast<float2*>(st + rb * ldst + cb * 128 + col) = make_float2(s0.s, s1.s);
 }
 
 // ---------------------------------------------------------------------------
@@ -146,12 +275,9 @@ __global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __res
 // contraction axis of the weight-gradient GEMM); codes are written transposed,
 // qt [C][R128] (ldqt), scales st [R128/128][C] (ldst). One CTA per 128x128
 // input block: the block is staged row-major in shared memory (coalesced
-// 16-byte loads, zero rows past R), then warp w takes rows 32 (w%4) .. +31 of
-// the column pairs 64 (w/4) + 2 lane, +1 (conflict-free 4-byte reads). The
-// four row quarters combine their partial amax through shared memory. Pad
-// rows R <= r < R128 hold +0 and so get code 0x00.
+// 16-byte loads, zero rows past R), then the column pass.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t R,
+__global__ void __launch_bounds__(256, 3) quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t R,
                                                               int64_t ldx, uint8_t* __restrict__ qt,
                                                               int64_t ldqt, float* __restrict__ st,
                                                               int64_t ldst)
@@ -175,47 +301,58 @@ __global__ void __launch_bounds__(256) quant_transpose_kernel(const uint16_t* __
         *reinterpret_cast<uint4*>(&tile[idx >> 4][(idx & 15) * 4]) = v[i];
     }
     __syncthreads();
+    column_pass(tile, part, cb, rb, qt, ldqt, st, ldst);
+}
 
-    const int warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;
-    const int col = (warp >> 2) * 64 + 2 * lane;  // first of the thread's two columns
-    uint32_t wv[32];
-    float a0 = 0.0f, a1 = 0.0f;
+// ---------------------------------------------------------------------------
+// Both layouts of one activation in a single pass over HBM: the 1x128 tiles
+// along the columns (q [R][C], s [C/128][R], as quant_act_kernel) and the
+// transposed tiles along the rows (qt [C][R128], st [R128/128][C], as
+// quant_transpose_kernel). One CTA per 128x128 block; thread t's i-th 16-byte
+// load holds 8 values of row t/16 + 16 i, so the 16 lanes of a half-warp own
+// one 1x128 row tile and reduce its amax with shuffles while the block is
+// staged in shared memory for the column pass.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256, 3) quant_dual_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t ldx,
+                                                         uint8_t* __restrict__ q, int64_t ldq,
+                                                         float* __restrict__ s, int64_t lds,
+                                                         uint8_t* __restrict__ qt, int64_t ldqt,
+                                                         float* __restrict__ st, int64_t ldst)
+{
+    __shared__ __align__(16) uint32_t tile[128][64];
+    __shared__ __align__(16) float part[4][128];
+    const int tid = threadIdx.x;
+    const int sub = tid & 15;
+    const int64_t cb = blockIdx.x, rb = blockIdx.y;
+
+    uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        wv[i] = tile[quarter * 32 + i][col >> 1];
-        a0 = fmaxf(a0, fabsf(bf16_lo(wv[i])));
-        a1 = fmaxf(a1, fabsf(bf16_hi(wv[i])));
+    for (int i = 0; i < 8; ++i) {
+        const int idx = tid + 256 * i;
+        const int row = idx >> 4;
+        const int64_t gr = rb * 128 + row;
+        v[i] = (gr < R) ? ld_stream_v4(x + gr * ldx + cb * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<float2*>(&part[quarter][col]) = make_float2(a0, a1);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = tid + 256 * i;
+        *reinterpret_cast<uint4*>(&tile[idx >> 4][sub * 4]) = v[i];
+    }
+    // row tiles (1x128 along the columns) from the registers
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = (tid >> 4) + 16 * i;
+        const int64_t gr = rb * 128 + row;
+        const float a = amax16(amax_v4(v[i]));
+        if (gr < R) {
+            const TileScale ts = tile_scale(a);
+            *reinterpret_cast<uint2*>(q + gr * ldq + cb * 128 + sub * 8) = codes8(v[i], ts);
+            if (sub == 0)
+                s[cb * lds + gr] = ts.s;
+        }
+    }
     __syncthreads();
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const float2 p = *reinterpret_cast<const float2*>(&part[qq][col]);
-        a0 = fmaxf(a0, p.x);
-        a1 = fmaxf(a1, p.y);
-    }
-    const float s0 = tile_scale(a0), s1 = tile_scale(a1);
-
-    // column col: low halves; column col+1: high halves. 32 rows -> 32 codes each.
-    uint32_t c0[8], c1[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t lo01 = codes2(__byte_perm(wv[4 * j], wv[4 * j + 1], 0x5410), s0);
-        const uint32_t lo23 = codes2(__byte_perm(wv[4 * j + 2], wv[4 * j + 3], 0x5410), s0);
-        const uint32_t hi01 = codes2(__byte_perm(wv[4 * j], wv[4 * j + 1], 0x7632), s1);
-        const uint32_t hi23 = codes2(__byte_perm(wv[4 * j + 2], wv[4 * j + 3], 0x7632), s1);
-        c0[j] = lo01 | (lo23 << 16);
-        c1[j] = hi01 | (hi23 << 16);
-    }
-    uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + quarter * 32;
-    uint8_t* out1 = out0 + ldqt;
-    reinterpret_cast<uint4*>(out0)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-    reinterpret_cast<uint4*>(out0)[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
-    reinterpret_cast<uint4*>(out1)[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
-    reinterpret_cast<uint4*>(out1)[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
-    if (quarter == 0)
-        *reinterpret_cast<float2*>(st + rb * ldst + cb * 128 + col) = make_float2(s0, s1);
+    column_pass(tile, part, cb, rb, qt, ldqt, st, ldst);
 }
 
 }  // namespace bfp8

@@ -84,6 +84,17 @@ int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw,
 int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64_t ldx,
                            uint8_t* qt, int64_t ldqt, float* st, int64_t ldst, void* stream);
 
+/* Both activation layouts in one pass over x: exactly the outputs of
+ * fp8_quantize_act(x, R, C, ldx, q, ldq, s, lds) and of
+ * fp8_quantize_transpose(x, R, C, ldx, qt, ldqt, st, ldst), reading x once.
+ * A training step needs both layouts of x (forward and weight-gradient GEMMs)
+ * and of dy (input- and weight-gradient GEMMs); this call saves one read of
+ * the BF16 tensor. Arguments, alignment rules and errors are the union of the
+ * two calls'. */
+int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, int64_t ldx,
+                               uint8_t* q, int64_t ldq, float* s, int64_t lds,
+                               uint8_t* qt, int64_t ldqt, float* st, int64_t ldst, void* stream);
+
 /* Forward GEMM, y = x W^T:
  *   y[m][n] = bf16( sum_kb sx[kb][m] * sw[n/128][kb] * sum_{k in kb} qx[m][k] qw[n][k] )
  *   qx [M][K] (ldqx), sx [K/128][M] (ldsx), qw [N][K] (ldqw), sw [N/128][K/128] dense,

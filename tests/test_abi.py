@@ -21,6 +21,7 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = bfp8.header_functions()
     assert set(names) >= {"fp8_quantize_act", "fp8_quantize_weight", "fp8_quantize_transpose",
+                          "fp8_quantize_act_transpose",
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
@@ -60,6 +61,14 @@ def test_quantiser_argument_checks(lib):
     assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 200, A, 128, s) == EINVAL  # ldqt < R128
     assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 264, A, 128, s) == EALIGN  # ldqt % 16
     assert lib.fp8_quantize_transpose(A, 200, 128, 128, A, 256, A + 4, 128, s) == EALIGN
+    dual = lib.fp8_quantize_act_transpose
+    assert dual(None, 0, 128, 128, None, 128, None, 0, None, 128, None, 128, s) == OK
+    assert dual(A, 200, 100, 128, A, 128, A, 200, A, 256, A, 128, s) == ESHAPE
+    assert dual(A, 200, 128, 128, A, 128, A, 200, A, 200, A, 128, s) == EINVAL   # ldqt < R128
+    assert dual(A, 200, 128, 128, A, 128, A, 100, A, 256, A, 128, s) == EINVAL   # lds < R
+    assert dual(A, 200, 128, 128, None, 128, A, 200, A, 256, A, 128, s) == EINVAL
+    assert dual(A, 200, 128, 128, A, 128, A, 200, A + 8, 256, A, 128, s) == EALIGN
+    assert dual(A + 2, 200, 128, 128, A, 128, A, 200, A, 256, A, 128, s) == EALIGN
 
 
 def test_gemm_argument_checks(lib):

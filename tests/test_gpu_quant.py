@@ -136,3 +136,66 @@ def test_strided_inputs_and_outputs():
     _same(qt[:, :128].cpu().numpy(), qo)
     _same(st[:, :384].cpu().numpy(), so)
     assert (qt[:, 128:].cpu().numpy() == 0xCD).all()
+
+
+# ------------------------------------------------------------------ both layouts in one pass
+def _gpu_dual(bits):
+    q, s, qt, st = bfp8.fp8_quantize_act_transpose(to_dev_bf16(bits))
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy(), qt.cpu().numpy(), st.cpu().numpy()
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (6, 256), (127, 128), (129, 384), (300, 640), (1000, 2048)])
+def test_dual_layouts_edge_shapes(R, C):
+    x = _special_input(R, C, 11 * R + C)
+    q, s, qt, st = _gpu_dual(x)
+    qo, so = oracle.quantize_act(x)
+    qto, sto = oracle.quantize_transpose(x)
+    _same(q, qo)
+    _same(s, so)
+    _same(qt, qto)
+    _same(st, sto)
+
+
+def _sweep_rows(seed):
+    """Rows of 1x128 tiles whose first element is the tile maximum and whose other 127 elements walk
+    through every positive BF16 value below it (random signs). The maxima include 448 * 2^k, where
+    the scale is a power of two and every quotient is exact (ties on the E4M3 grid are hit exactly),
+    and random BF16 values, where quotients land anywhere between grid points."""
+    rng = np.random.default_rng(seed)
+    all_pos = np.arange(1, 0x7F80, dtype=np.uint16)            # every positive finite BF16 pattern
+    maxima = [wl.bf16_bits(np.float32(448.0 * 2.0 ** k)).item() for k in (-20, -3, 0, 5)]
+    maxima += list(rng.integers(0x3000, 0x4A00, size=12).astype(np.uint16))
+    rows = []
+    for m in maxima:
+        vals = all_pos[all_pos < m]
+        vals = np.concatenate([vals, vals[:(-len(vals)) % 127]])  # pad to whole rows
+        body = vals.reshape(-1, 127)
+        signs = (rng.random(body.shape) < 0.5).astype(np.uint16) << 15
+        body = body | signs
+        head = np.full((body.shape[0], 1), m, dtype=np.uint16)
+        rows.append(np.concatenate([head, body], axis=1))
+    return np.concatenate(rows, axis=0)
+
+
+def test_codes_bit_exact_over_every_bf16_value():
+    """The kernels compute fl32(x * fl32(1/s)) and fall back to the IEEE quotient near E4M3 rounding
+    boundaries; every BF16 value below each tile maximum must still give the definition's code."""
+    x = _sweep_rows(5)
+    q, s = _gpu_act(x)
+    qo, so = oracle.quantize_act(x)
+    _same(q, qo)
+    _same(s, so)
+    # the same values down the columns (transposed tiles, and both layouts at once)
+    R = x.shape[0] // 128 * 128
+    xt = np.ascontiguousarray(x[:R].T)  # column i of xt is row i of x
+    qt, st = _gpu_transpose(xt)
+    qto, sto = oracle.quantize_transpose(xt)
+    _same(qt, qto)
+    _same(st, sto)
+    q, s, qt, st = _gpu_dual(xt)
+    _same(qt, qto)
+    _same(st, sto)
+    qo, so = oracle.quantize_act(xt)
+    _same(q, qo)
+    _same(s, so)
