@@ -245,8 +245,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::BM, Cfg::BN, Cfg::B_MN);
-            const uint32_t a_base = smem_u32(sA);
-            const uint32_t b_base = smem_u32(sB);
+            // Descriptors of stage 0, K step 0; the others differ only in the start
+            // address field (bits 0-13, in 16-byte units), which never carries over
+            // because shared-memory addresses stay below 256 KB.
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+            const uint64_t b_desc0 = Cfg::B_MN ? smem_desc_sw128(smem_u32(sB), 128 * Cfg::BK, 1024)
+                                               : smem_desc_sw128(smem_u32(sB), 16, 1024);
+            constexpr uint32_t kBStep = Cfg::B_MN ? 32 * 128 : 32;  // bytes per K step of 32
             for (int g = 0; g < my_chunks; ++g) {
                 const int s = g % Cfg::STAGES;
                 const uint32_t ph = (g / Cfg::STAGES) & 1;
@@ -258,14 +263,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::BN;
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * Cfg::A_BYTES) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 32; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(a_base + s * Cfg::A_BYTES + kk * 32, 16, 1024);
-                    const uint64_t bd =
-                        Cfg::B_MN ? smem_desc_sw128(b_base + s * Cfg::B_BYTES + kk * 32 * 128, 128 * Cfg::BK, 1024)
-                                  : smem_desc_sw128(b_base + s * Cfg::B_BYTES + kk * 32, 16, 1024);
-                    mma_e4m3(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < Cfg::BK / 32; ++kk)
+                    mma_e4m3(d_tmem, ad + (kk * 32) / 16, bd + (kk * kBStep) / 16, idesc, kk > 0 ? 1u : 0u);
                 mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
             }

@@ -9,21 +9,24 @@
 // codes. Both divisions are IEEE binary32 divisions, so codes and scales are
 // reproducible bit for bit.
 //
-// Exact codes without a division per element. Let r = fl32(1/s) and
-// t = fl32(x * r). Each of the two roundings is off by a relative 2^-24 at
-// most, so t is within 2 units in the last place (ulp) of the exact quotient
-// x/s, and within 3 ulp of fl32(x/s). The E4M3 code of a binary32 value only
-// changes where the value crosses a rounding boundary of the E4M3 grid: in the
-// normal E4M3 range (|t| >= 2^-6) those boundaries are the binary32 numbers
-// whose low 20 mantissa bits are 0x80000 (the midpoint between two codes with
-// 3 mantissa bits). If t's low 20 bits are more than 4 units away from that
-// pattern, t and fl32(x/s) lie on the same side of every boundary and encode to
-// the same code. Below 2^-11 both encode to a signed zero (the smallest
-// non-zero code is 2^-9, so the boundary is 2^-10). Everything else - values
-// within 4 ulp of a boundary, the subnormal E4M3 range [2^-11, 2^-6), and tiles
-// whose scale is a binary32 subnormal (1/s may then overflow) - takes the IEEE
-// division. The slow path is rare (about one element in 10^4 for normal data)
-// and only changes which instructions compute fl32(x/s), never the result.
+// Exact quotients without a division instruction per element (Markstein's
+// method: P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also the Handbook of
+// Floating-Point Arithmetic, Muller et al., section on division with an FMA).
+// With y = RN(1/s) (one correctly rounded reciprocal per tile) and the
+// remainder r = a - s q, which an FMA computes exactly when q is within an ulp
+// of a/s and nothing underflows, the step q' = RN(q + r y) returns RN(a/s)
+// whenever q is a faithful approximation of a/s. The first product q0 = RN(a y)
+// is within 1.5 ulp of a/s, so one step first brings it within a hair of a/s
+// (faithful), and a second step makes it the correctly rounded quotient,
+// identical to the IEEE division. To keep the remainders clear of the
+// subnormal range, tiles with a scale below 2^-60 (including binary32
+// subnormal scales) work on a and s both multiplied by 2^64, which changes
+// neither the quotient nor any rounding. The quotient is taken of |x| and given
+// x's sign afterwards, so that -0 keeps its sign; an all-zero tile (s = 0)
+// runs the same instructions with y = 0 and yields the inputs' signed zeros.
+// Where a is so small against s that a remainder still underflows, the
+// quotient is below 2^-40 and its code is a signed zero either way.
 //
 // All four kernels are HBM-bound (2 B read + 1 B written per element and per
 // code layout): reads are 16-byte vector loads that cover whole 128-byte lines,
@@ -37,59 +40,44 @@
 
 namespace bfp8 {
 
-// A tile's scale and, when usable, its reciprocal.
+// A tile's scale and what the division-free quotient needs.
 struct TileScale {
-    float s;   // fl32(amax / 448), 0 for an all-zero tile
-    float r;   // fl32(1 / s) if s is a normal binary32 number
-    bool fast; // r is usable
+    float s;    // fl32(amax / 448), 0 for an all-zero tile: the stored scale
+    float pre;  // 2^64 for tiny scales, else 1 (applied to both operands)
+    float sp;   // s * pre (exact), or 1 for an all-zero tile
+    float y;    // RN(1 / sp), or 0 for an all-zero tile
 };
 
 __device__ __forceinline__ TileScale tile_scale(float amax)
 {
     TileScale t;
     t.s = __fdiv_rn(amax, 448.0f);
-    t.fast = t.s >= 1.17549435e-38f;  // smallest normal binary32
-    t.r = t.fast ? __frcp_rn(t.s) : 0.0f;
+    t.pre = t.s < 0x1p-60f ? 0x1p64f : 1.0f;
+    t.sp = t.s == 0.0f ? 1.0f : t.s * t.pre;
+    t.y = t.s == 0.0f ? 0.0f : __frcp_rn(t.sp);
     return t;
 }
 
-// True if the E4M3 code of t equals that of fl32(x / s) (see the header comment).
-__device__ __forceinline__ bool quotient_safe(float t)
+// RN(x / s) by two Markstein steps.
+__device__ __forceinline__ float quotient(float x, const TileScale& ts)
 {
-    const uint32_t u = __float_as_uint(t) & 0x7FFFFFFFu;
-    const bool tiny = u < 0x3A000000u;                            // |t| < 2^-11: code +-0
-    const bool normal = u >= 0x3C800000u;                         // |t| >= 2^-6
-    const bool far = ((u & 0xFFFFFu) - 0x7FFFCu) > 8u;            // not within 4 ulp of a midpoint
-    return tiny || (normal && far);
+    const float a = fabsf(x) * ts.pre;
+    float q = a * ts.y;
+    float r = fmaf(-q, ts.sp, a);
+    q = fmaf(r, ts.y, q);
+    r = fmaf(-q, ts.sp, a);
+    q = fmaf(r, ts.y, q);
+    return copysignf(q, x);
 }
 
-// fl32(x / s), the definition's quotient, by the exact route. Kept out of line
-// so that the compiler cannot evaluate the division speculatively on the
-// fast path; it only runs for the rare values that need it.
-__device__ __noinline__ float exact_quotient(float x, float s, float t, bool fast)
-{
-    if (fast && quotient_safe(t))
-        return t;
-    // all-zero tile: every x is +-0 and its code is the signed zero itself
-    return s == 0.0f ? x : __fdiv_rn(x, s);
-}
-
-// Codes of N values (N even); out[i] packs codes 4i .. 4i+3, first value in the low byte.
+// Codes of N values (N a multiple of 4); out[i] packs codes 4i .. 4i+3, first value in the low byte.
 template <int N>
 __device__ __forceinline__ void encode(const float (&x)[N], const TileScale& ts, uint32_t (&out)[N / 4])
 {
     float t[N];
-    bool ok = ts.fast;
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        t[i] = x[i] * ts.r;
-        ok = ok & quotient_safe(t[i]);
-    }
-    if (!ok) {
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-            t[i] = exact_quotient(x[i], ts.s, t[i], ts.fast);
-    }
+    for (int i = 0; i < N; ++i)
+        t[i] = quotient(x[i], ts);
 #pragma unroll
     for (int i = 0; i < N / 4; ++i)
         out[i] = cvt_e4m3x2(t[4 * i], t[4 * i + 1]) | (cvt_e4m3x2(t[4 * i + 2], t[4 * i + 3]) << 16);

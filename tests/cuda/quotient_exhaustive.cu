@@ -1,0 +1,67 @@
+// Exhaustive check of the quantisers' division-free quotient (quant.cuh) against
+// the IEEE binary32 division, over the whole input domain the kernels can see:
+// every finite BF16 tile maximum `amax` >= 0 (s = RN(amax/448)) and every finite
+// BF16 value x with |x| <= amax. Two counts, both must be zero:
+//   code mismatches: E4M3 code of the quotient differs from that of x / s;
+//   quotient mismatches: the quotient's bits differ from x / s, counted where
+//     |x / s| >= 2^-12 (below 2^-10 every code is a signed zero).
+// For an all-zero tile (amax = 0) the definition's quotient is x itself.
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "quant.cuh"
+
+__global__ void check(unsigned long long* pairs, unsigned long long* bad, unsigned* first)
+{
+    const unsigned ab = blockIdx.y;  // amax bit pattern (0 .. largest finite)
+    const float amax = __uint_as_float(ab << 16);
+    const bfp8::TileScale ts = bfp8::tile_scale(amax);
+    unsigned long long n = 0;
+    for (unsigned xb = blockIdx.x * blockDim.x + threadIdx.x; xb < 65536u; xb += gridDim.x * blockDim.x) {
+        if ((xb & 0x7FFFu) > ab)
+            continue;  // |x| > amax never occurs in a tile
+        const float x = __uint_as_float(xb << 16);
+        const float q = bfp8::quotient(x, ts);
+        const float d = ts.s == 0.0f ? x : __fdiv_rn(x, ts.s);
+        ++n;
+        const bool code_differs = bfp8::cvt_e4m3x2(q, 0.0f) != bfp8::cvt_e4m3x2(d, 0.0f);
+        const bool quot_differs = fabsf(d) >= 0x1p-12f && __float_as_uint(q) != __float_as_uint(d);
+        if (code_differs || quot_differs) {
+            const unsigned long long k = atomicAdd(bad, 1ull);
+            if (k < 4) {
+                first[3 * k] = xb;
+                first[3 * k + 1] = ab;
+                first[3 * k + 2] = __float_as_uint(q);
+            }
+        }
+    }
+    atomicAdd(pairs, n);
+}
+
+int main()
+{
+    unsigned long long *dpairs = nullptr, *dbad = nullptr;
+    unsigned* dfirst = nullptr;
+    if (cudaMalloc(&dpairs, 8) != cudaSuccess || cudaMalloc(&dbad, 8) != cudaSuccess ||
+        cudaMalloc(&dfirst, 12 * sizeof(unsigned)) != cudaSuccess)
+        return 3;
+    cudaMemset(dpairs, 0, 8);
+    cudaMemset(dbad, 0, 8);
+    const dim3 grid(32, 0x7F80);  // x blocks, every finite amax pattern 0x0000 .. 0x7F7F
+    check<<<grid, 256>>>(dpairs, dbad, dfirst);
+    unsigned long long pairs = 0, bad = 0;
+    unsigned first[12] = {};
+    cudaError_t err = cudaMemcpy(&pairs, dpairs, 8, cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(&bad, dbad, 8, cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(first, dfirst, sizeof first, cudaMemcpyDeviceToHost);
+    printf("pairs %llu mismatches %llu status %s\n", pairs, bad, cudaGetErrorString(err));
+    for (unsigned i = 0; i < bad && i < 4; ++i)
+        printf("  x=%04x amax=%04x quotient=%08x\n", first[3 * i], first[3 * i + 1], first[3 * i + 2]);
+    cudaFree(dpairs);
+    cudaFree(dbad);
+    cudaFree(dfirst);
+    return (err == cudaSuccess && bad == 0 && pairs > 0) ? 0 : 2;
+}
