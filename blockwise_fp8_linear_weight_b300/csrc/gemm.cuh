@@ -28,15 +28,18 @@
 //               and BN/2 columns; per chunk it reads the partial sums with
 //               tcgen05.ld (two loads in flight per wait), releases the TMEM
 //               buffer and accumulates  acc += partial * (sA * sB)  in FP32
-//               registers; after the last chunk of a
+//               registers with packed two-lane FP32 instructions (scalar FP32
+//               instructions issued at this rate halve the tensor core's MMA
+//               rate on sm_103; the packed form leaves it at full speed); after
+//               the last chunk of a
 //               tile it rounds acc to BF16, stages it in its own 128-byte-
 //               swizzled shared-memory slab and issues TMA stores (the TMA unit
 //               drops rows and columns outside D), overlapping the MMAs of the
 //               next tile.
 // With BN = 256 the promotion warps need more than the 168 registers a
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
-// warpgroup (40 each) to the promotion warpgroups (232 each):
-// 128 x 40 + 256 x 232 = 384 x 168.
+// warpgroup to the promotion warpgroups (56/224, or 64/216 with per-column
+// B scales), within the launch budget of 384 x 168.
 // Every mbarrier wait is bounded (mbar_wait); a timeout sets the library's
 // device status word and the kernel unwinds without hanging.
 #pragma once
@@ -44,13 +47,6 @@
 #include <cstdint>
 
 #include "ptx.cuh"
-
-// Promotion arithmetic: 1 = packed two-lane FP32 instructions, 0 = scalar FMA.
-// The packed form issues half the instructions but the FP32 pipe processes the
-// same number of lanes per clock, so it is off by default.
-#ifndef BFP8_PROMO_F32X2
-#define BFP8_PROMO_F32X2 0
-#endif
 
 namespace bfp8 {
 
@@ -91,7 +87,11 @@ struct GemmConfig {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     // registers per thread at launch (65536 / 384, rounded down to a multiple of 8)
     static constexpr int LAUNCH_REGS = 168;
-    static_assert(!REG_SPLIT || 128 * 40 + 256 * 232 <= THREADS * LAUNCH_REGS, "register split");
+    // setmaxnreg split between the producer/MMA warpgroup and the two promotion
+    // warpgroups (chosen so that neither side spills on its hot path)
+    static constexpr int REG_LOW = SB_VEC ? 64 : 56;
+    static constexpr int REG_HIGH = SB_VEC ? 216 : 224;
+    static_assert(!REG_SPLIT || 128 * REG_LOW + 256 * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
 };
 
 struct GemmArgs {
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // allocates every role's code under that role's budget.
     if (warp < 4) {
         if (Cfg::REG_SPLIT)
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REG_LOW));
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     } else {
         if (Cfg::REG_SPLIT)
-            asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REG_HIGH));
         // ---------------------------------------------------------------- promotion + epilogue
         constexpr int CPW = Cfg::CPW;
         const int pw = warp - 4;            // 0 .. 7
@@ -288,25 +288,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int row = quarter * 32 + lane;
         uint8_t* my_out = sOut + pw * (CPW / 64) * Cfg::BOX_BYTES;
 
-        float acc[CPW];
+        // FP32 accumulators of the thread's row, as packed pairs of neighbouring columns
+        uint64_t acc[CPW / 2];
 #pragma unroll
-        for (int i = 0; i < CPW; ++i)
-            acc[i] = 0.0f;
+        for (int i = 0; i < CPW / 2; ++i)
+            acc[i] = 0;
 
-        // scalar-mode B scale of chunk g (one value per warp), fetched two chunks ahead
-        auto load_sb = [&](int g) -> float {
-            if (Cfg::SB_VEC || g >= my_chunks)
-                return 0.0f;
-            const int tt = g / nc, cc = g - tt * nc;
-            int mm, nn;
-            tile_origin<Cfg>(args, tt, mm, nn);
-            const int col = nn + half * CPW;
-            if (col >= args.gn)
-                return 0.0f;
-            return __ldg(args.sb_scalar + static_cast<int64_t>(col / 128) * args.sb_col_stride +
-                         static_cast<int64_t>(cc) * args.sb_chunk_stride);
+        // Scalar-mode B scale (one value per warp and chunk), fetched two chunks
+        // ahead by a cursor that walks the chunks in order; the tile origin is
+        // recomputed once per tile, not per chunk.
+        int sb_t = 0, sb_c_idx = 0, sb_m0 = 0, sb_n0 = 0;
+        tile_origin<Cfg>(args, 0, sb_m0, sb_n0);
+        auto next_sb = [&]() -> float {
+            float v = 0.0f;
+            if (!Cfg::SB_VEC && sb_t < my_tiles) {
+                const int col = sb_n0 + half * CPW;
+                if (col < args.gn)
+                    v = __ldg(args.sb_scalar + static_cast<int64_t>(col >> 7) * args.sb_col_stride +
+                              static_cast<int64_t>(sb_c_idx) * args.sb_chunk_stride);
+                if (++sb_c_idx == nc) {
+                    sb_c_idx = 0;
+                    ++sb_t;
+                    tile_origin<Cfg>(args, sb_t, sb_m0, sb_n0);
+                }
+            }
+            return v;
         };
-        float sb0 = load_sb(0), sb1 = load_sb(1);
+        float sb0 = next_sb();
+        float sb1 = next_sb();
 
         int t = 0, c = 0, m0 = 0, n0 = 0;
         tile_origin<Cfg>(args, 0, m0, n0);
@@ -317,78 +326,43 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t bph = (g >> 1) & 1;
             const float sb_c = sb0;
             sb0 = sb1;
-            sb1 = load_sb(g + 2);
+            sb1 = next_sb();
             if (!mbar_wait(&sfull[ss], sph, abort_flag, args.status))
                 break;
             if (!mbar_wait(&tfull[b], bph, abort_flag, args.status))
                 break;
             tc_fence_after_sync();
             const float sa = sSA[ss * Cfg::BM + row];
+            const uint64_t sa2 = pack_f32x2(sa, sa);
             const float sc = sa * sb_c;
+            const uint64_t sc2 = pack_f32x2(sc, sc);
             const uint32_t t_base =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BN + half * CPW;
 #pragma unroll
             for (int j = 0; j < CPW / 64; ++j) {
-                uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(t_base + j * 64, r0);
-                tmem_ld_32x32b_x32(t_base + j * 64 + 32, r1);
-                tmem_ld_wait();
+                uint64_t p[32];  // columns j*64 .. j*64+63 of the partial sums, as pairs
+                tmem_ld_x64_pairs(t_base + j * 64, p);
                 if (j == CPW / 64 - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&tempty[b]);
                 }
-                float* a = acc + j * 64;
+                uint64_t* a = acc + j * 32;
                 if (Cfg::SB_VEC) {
-                    // per-column scales: broadcast 16-byte shared-memory reads
-                    const float4* sbv = reinterpret_cast<const float4*>(sSB + ss * Cfg::BN + half * CPW + j * 64);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 v0 = sbv[i];
-                        const float4 v1 = sbv[8 + i];
-                        float p[8];
-#if BFP8_PROMO_F32X2
-                        fmul2(p[0], p[1], __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]), v0.x, v0.y);
-                        fmul2(p[2], p[3], __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]), v0.z, v0.w);
-                        fmul2(p[4], p[5], __uint_as_float(r1[4 * i]), __uint_as_float(r1[4 * i + 1]), v1.x, v1.y);
-                        fmul2(p[6], p[7], __uint_as_float(r1[4 * i + 2]), __uint_as_float(r1[4 * i + 3]), v1.z, v1.w);
-                        ffma2(a[4 * i], a[4 * i + 1], p[0], p[1], sa, sa);
-                        ffma2(a[4 * i + 2], a[4 * i + 3], p[2], p[3], sa, sa);
-                        ffma2(a[32 + 4 * i], a[32 + 4 * i + 1], p[4], p[5], sa, sa);
-                        ffma2(a[32 + 4 * i + 2], a[32 + 4 * i + 3], p[6], p[7], sa, sa);
-#else
-                        p[0] = __uint_as_float(r0[4 * i]) * v0.x;
-                        p[1] = __uint_as_float(r0[4 * i + 1]) * v0.y;
-                        p[2] = __uint_as_float(r0[4 * i + 2]) * v0.z;
-                        p[3] = __uint_as_float(r0[4 * i + 3]) * v0.w;
-                        p[4] = __uint_as_float(r1[4 * i]) * v1.x;
-                        p[5] = __uint_as_float(r1[4 * i + 1]) * v1.y;
-                        p[6] = __uint_as_float(r1[4 * i + 2]) * v1.z;
-                        p[7] = __uint_as_float(r1[4 * i + 3]) * v1.w;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            a[4 * i + k] = fmaf(p[k], sa, a[4 * i + k]);
-                            a[32 + 4 * i + k] = fmaf(p[4 + k], sa, a[32 + 4 * i + k]);
-                        }
-#endif
-                    }
-                } else {
-#if BFP8_PROMO_F32X2
+                    // per-column scales: broadcast 16-byte shared-memory reads (two column pairs each)
+                    const ulonglong2* sbv =
+                        reinterpret_cast<const ulonglong2*>(sSB + ss * Cfg::BN + half * CPW + j * 64);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        ffma2(a[2 * i], a[2 * i + 1], __uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
-                              sc, sc);
-                        ffma2(a[32 + 2 * i], a[32 + 2 * i + 1], __uint_as_float(r1[2 * i]),
-                              __uint_as_float(r1[2 * i + 1]), sc, sc);
+                        const ulonglong2 v = sbv[i];
+                        ffma2(a[2 * i], fmul2(p[2 * i], v.x), sa2);
+                        ffma2(a[2 * i + 1], fmul2(p[2 * i + 1], v.y), sa2);
                     }
-#else
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        a[i] = fmaf(__uint_as_float(r0[i]), sc, a[i]);
-                        a[32 + i] = fmaf(__uint_as_float(r1[i]), sc, a[32 + i]);
-                    }
-#endif
+                    for (int i = 0; i < 32; ++i)
+                        ffma2(a[i], p[i], sc2);
                 }
             }
             // this warp is done with the chunk's scales
@@ -407,12 +381,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float* v = acc + bx * 64 + k * 8;
+                        const uint64_t* v = acc + bx * 32 + k * 4;
                         uint4 pk;
-                        pk.x = cvt_bf16x2(v[0], v[1]);
-                        pk.y = cvt_bf16x2(v[2], v[3]);
-                        pk.z = cvt_bf16x2(v[4], v[5]);
-                        pk.w = cvt_bf16x2(v[6], v[7]);
+                        pk.x = cvt_bf16x2(v[0]);
+                        pk.y = cvt_bf16x2(v[1]);
+                        pk.z = cvt_bf16x2(v[2]);
+                        pk.w = cvt_bf16x2(v[3]);
                         *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
                     }
                 }
@@ -426,8 +400,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tma_store_commit();
                 }
 #pragma unroll
-                for (int i = 0; i < CPW; ++i)
-                    acc[i] = 0.0f;
+                for (int i = 0; i < CPW / 2; ++i)
+                    acc[i] = 0;
                 c = 0;
                 ++t;
                 tile_origin<Cfg>(args, t, m0, n0);

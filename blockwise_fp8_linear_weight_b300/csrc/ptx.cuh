@@ -87,6 +87,43 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_wait, but polls with the non-suspending test_wait: the thread sees
+// the phase complete within a few cycles instead of whenever a suspended
+// try_wait is resumed. Meant for a single latency-critical thread.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                               unsigned* status)
+{
+    if (mbar_test_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
@@ -242,35 +279,87 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// 32 lanes x 64 consecutive 32-bit columns starting at taddr, waited for, and
+// returned as 32 packed pairs of neighbouring columns (column 2i in the low
+// word of p[i]). Loading, waiting and pairing in one block lets the register
+// allocator place each pair in a 64-bit register directly, so the packed FP32
+// instructions that consume them need no register moves.
+__device__ __forceinline__ void tmem_ld_x64_pairs(uint32_t taddr, uint64_t (&p)[32])
+{
+    asm volatile(
+        "{\n\t.reg .b32 r<64>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, "
+        "r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31, "
+        "r32, r33, r34, r35, r36, r37, r38, r39, r40, r41, r42, r43, r44, r45, r46, r47, "
+        "r48, r49, r50, r51, r52, r53, r54, r55, r56, r57, r58, r59, r60, r61, r62, r63}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
+        "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t"
+        "mov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
+        "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\t"
+        "mov.b64 %16, {r32, r33};\n\tmov.b64 %17, {r34, r35};\n\tmov.b64 %18, {r36, r37};\n\tmov.b64 %19, {r38, r39};\n\t"
+        "mov.b64 %20, {r40, r41};\n\tmov.b64 %21, {r42, r43};\n\tmov.b64 %22, {r44, r45};\n\tmov.b64 %23, {r46, r47};\n\t"
+        "mov.b64 %24, {r48, r49};\n\tmov.b64 %25, {r50, r51};\n\tmov.b64 %26, {r52, r53};\n\tmov.b64 %27, {r54, r55};\n\t"
+        "mov.b64 %28, {r56, r57};\n\tmov.b64 %29, {r58, r59};\n\tmov.b64 %30, {r60, r61};\n\tmov.b64 %31, {r62, r63};\n\t}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]),
+          "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]),
+          "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]),
+          "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// d = a * s on packed pairs
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t s)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(s));
+    return d;
+}
+
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ packed FP32 arithmetic
-// Two-lane FP32 operations (one instruction for two independent values, each
-// rounded to nearest-even exactly like the scalar operation).
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1)
+// Two FP32 values travel as one 64-bit register pair (low word = first value)
+// and are processed by one instruction; each lane is rounded to nearest-even
+// exactly like the scalar operation.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
 {
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rd, {%0, %1};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
 
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1)
+// acc = {lo, hi} * s + acc  (lo, hi: raw FP32 bits, e.g. from tcgen05.ld)
+__device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint32_t lo, uint32_t hi, uint64_t s)
 {
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+    asm("{\n\t.reg .b64 p;\n\t"
+        "mov.b64 p, {%1, %2};\n\t"
+        "fma.rn.f32x2 %0, p, %3, %0;\n\t}"
+        : "+l"(acc)
+        : "r"(lo), "r"(hi), "l"(s));
+}
+
+// {lo, hi} * s
+__device__ __forceinline__ uint64_t fmul2(uint32_t lo, uint32_t hi, uint64_t s)
+{
+    uint64_t d;
+    asm("{\n\t.reg .b64 p;\n\t"
+        "mov.b64 p, {%1, %2};\n\t"
+        "mul.rn.f32x2 %0, p, %3;\n\t}"
+        : "=l"(d)
+        : "r"(lo), "r"(hi), "l"(s));
+    return d;
+}
+
+// acc = a * s + acc
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t a, uint64_t s)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(s));
 }
 
 // ------------------------------------------------------------------ conversions
@@ -288,6 +377,18 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi)
 {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A packed FP32 pair -> packed BF16x2 (round to nearest-even), low value in the low half.
+__device__ __forceinline__ uint32_t cvt_bf16x2(uint64_t v)
+{
+    uint32_t r;
+    asm("{\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %1;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "l"(v));
     return r;
 }
 
