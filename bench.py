@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 256], help="GEMM tile width (0: automatic)")
+    p.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2], help="GEMM CTAs per cluster (0: automatic)")
     return p.parse_args()
 
 
@@ -240,6 +242,8 @@ def run_ours(args):
     from blockwise_fp8_linear_weight_b300 import build as lib_build
     lib_build.build()
     bfp8.load_library()
+    bfp8.set_gemm_tile_n(args.gemm_tile_n)
+    bfp8.set_gemm_cluster(args.gemm_cluster)
 
     work = workload(args.workload)
     dev = torch.device("cuda", local)

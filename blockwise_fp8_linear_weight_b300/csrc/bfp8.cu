@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -26,6 +27,7 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;  // TMA coordinates are in
 constexpr int64_t kMaxGridY = 65535;
 
 std::atomic<int> g_tile_n{0};
+std::atomic<int> g_cluster{0};
 
 // ----------------------------------------------------------------- helpers
 bool aligned(const void* p, uintptr_t a)
@@ -138,6 +140,37 @@ struct GemmProblem {
     int64_t gm, gn, gk;
 };
 
+// Clusters of this kernel that fit on the device at once (one CTA per SM), cached.
+template <class Cfg>
+int max_clusters(int dev)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        n = sm_count(dev) / Cfg::CLUSTER;
+        if (Cfg::CLUSTER > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(n * Cfg::CLUSTER));
+            cfg.blockDim = dim3(Cfg::THREADS);
+            cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = Cfg::CLUSTER;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int active = 0;
+            if (cudaOccupancyMaxActiveClusters(&active, bfp8_gemm_kernel<Cfg>, &cfg) == cudaSuccess && active > 0)
+                n = std::min(n, active);
+        }
+        if (n < 1)
+            n = 1;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 template <class Cfg>
 int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int dev)
 {
@@ -149,7 +182,7 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
         ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gn, p.gk, p.ldb, 128, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     else
-        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN,
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN / Cfg::CLUSTER,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, 1,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -188,13 +221,29 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     // sweep along N first when B is the smaller operand (it then stays in L2
     // while the larger A is streamed once), along M otherwise
     args.n_fastest = p.gn < p.gm ? 1 : 0;
+    args.d = static_cast<uint16_t*>(p.d);
+    args.ldd = p.ldd;
     args.sb_scalar = p.sb;
     args.sb_col_stride = p.sb_col_stride;
     args.sb_chunk_stride = p.sb_chunk_stride;
     args.status = status;
-    const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
-    const int ctas = static_cast<int>(tiles < sm_count(dev) ? tiles : sm_count(dev));
-    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
+    const int64_t super_tiles =
+        static_cast<int64_t>((args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER) * args.tiles_n;
+    const int clusters = static_cast<int>(std::min<int64_t>(super_tiles, max_clusters<Cfg>(dev)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * Cfg::CLUSTER));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmSB, tmD, args) != cudaSuccess)
+        return BFP8_ELAUNCH;
     return launch_status();
 }
 
@@ -211,9 +260,14 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
     int tn = g_tile_n.load(std::memory_order_relaxed);
     if (tn == 0)
         tn = 256;
-    if (tn == 256)
-        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC>>(p, status, stream, dev);
-    return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
+    if (tn == 128)
+        return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
+    int cl = g_cluster.load(std::memory_order_relaxed);
+    if (cl == 0)
+        cl = 1;  // measured: multicast halves L2 traffic but the path is not L2-bound
+    if (cl == 2)
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 2>>(p, status, stream, dev);
+    return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1>>(p, status, stream, dev);
 }
 
 bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)
@@ -226,6 +280,44 @@ bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)
 }  // namespace bfp8
 
 using namespace bfp8;
+
+namespace bfp8 {
+namespace {
+
+// Launches the persistent block quantiser over x [R][C] (C % 128 == 0, R >= 1).
+template <int MODE>
+int run_quant_blocks(const void* x, int64_t R, int64_t C, int64_t ldx, const QuantArgs& base, cudaStream_t stream)
+{
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    unsigned* status = device_status_ptr(dev);
+    if (!status)
+        return BFP8_ELAUNCH;
+    CUtensorMap tm;
+    if (!make_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(C), static_cast<uint64_t>(R),
+                  static_cast<uint64_t>(ldx) * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return BFP8_ELAUNCH;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    auto kern = quant_blocks_kernel<MODE>;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmemBytes) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    QuantArgs a = base;
+    a.R = R;
+    a.nblk_c = C / 128;
+    a.nblocks = ((R + 127) / 128) * a.nblk_c;
+    a.status = status;
+    const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * 3);
+    kern<<<static_cast<unsigned>(ctas), 256, kQuantSmemBytes, stream>>>(tm, a);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace bfp8
 
 // =================================================================== quantisers
 extern "C" int fp8_quantize_act(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q, int64_t ldq,
@@ -244,13 +336,12 @@ extern "C" int fp8_quantize_act(const void* x, int64_t R, int64_t C, int64_t ldx
     int rc = check_arch(nullptr);
     if (rc != BFP8_OK)
         return rc;
-    const int64_t nchunks = C / 128;
-    const int64_t ntiles = R * nchunks;
-    constexpr int UNROLL = 4;
-    const int64_t blocks = (ntiles + 16 * UNROLL - 1) / (16 * UNROLL);
-    quant_act_kernel<UNROLL><<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), ldx, q, ldq, s, lds, nchunks, ntiles);
-    return launch_status();
+    QuantArgs qa{};
+    qa.q = q;
+    qa.ldq = ldq;
+    qa.s = s;
+    qa.lds = lds;
+    return run_quant_blocks<MODE_ROWS>(x, R, C, ldx, qa, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
@@ -269,10 +360,12 @@ extern "C" int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t 
     int rc = check_arch(nullptr);
     if (rc != BFP8_OK)
         return rc;
-    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
-    quant_weight_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint16_t*>(w), ldw,
-                                                                             q, ldq, s, K / 128);
-    return launch_status();
+    QuantArgs qa{};
+    qa.q = q;
+    qa.ldq = ldq;
+    qa.s = s;
+    qa.lds = K / 128;
+    return run_quant_blocks<MODE_WEIGHT>(w, N, K, ldw, qa, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* qt,
@@ -292,10 +385,12 @@ extern "C" int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64
     int rc = check_arch(nullptr);
     if (rc != BFP8_OK)
         return rc;
-    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R128 / 128));
-    quant_transpose_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), R, ldx, qt, ldqt, st, ldst);
-    return launch_status();
+    QuantArgs qa{};
+    qa.qt = qt;
+    qa.ldqt = ldqt;
+    qa.st = st;
+    qa.ldst = ldst;
+    return run_quant_blocks<MODE_COLS>(x, R, C, ldx, qa, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
@@ -317,10 +412,16 @@ extern "C" int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, i
     int rc = check_arch(nullptr);
     if (rc != BFP8_OK)
         return rc;
-    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(R128 / 128));
-    quant_dual_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), R, ldx, q, ldq, s, lds, qt, ldqt, st, ldst);
-    return launch_status();
+    QuantArgs qa{};
+    qa.q = q;
+    qa.ldq = ldq;
+    qa.s = s;
+    qa.lds = lds;
+    qa.qt = qt;
+    qa.ldqt = ldqt;
+    qa.st = st;
+    qa.ldst = ldst;
+    return run_quant_blocks<MODE_DUAL>(x, R, C, ldx, qa, static_cast<cudaStream_t>(stream));
 }
 
 // =================================================================== GEMMs
@@ -466,6 +567,13 @@ extern "C" int bfp8_last_device_status(void* stream)
         cudaStreamSynchronize(st) != cudaSuccess)
         return BFP8_ELAUNCH;
     return (host & kDevTimeout) ? BFP8_ETIMEOUT : BFP8_OK;
+}
+
+extern "C" int bfp8_set_gemm_cluster(int cluster)
+{
+    if (cluster != 0 && cluster != 1 && cluster != 2)
+        return BFP8_EINVAL;
+    return g_cluster.exchange(cluster);
 }
 
 extern "C" int bfp8_set_gemm_tile_n(int tile_n)

@@ -50,7 +50,7 @@
 
 namespace bfp8 {
 
-template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_>
+template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, bool EPI_SMEM_ = true>
 struct GemmConfig {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -59,11 +59,23 @@ struct GemmConfig {
     static constexpr int SSTAGES = 8;
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
+    // epilogue: true = stage BF16 tiles in shared memory and store them with TMA
+    // (default); false = each thread stores its row's 16-byte groups straight to
+    // global memory, which frees the staging slab for a deeper operand ring but
+    // measured slower (the uncoalesced stores hold up the promotion warps)
+    static constexpr bool EPI_SMEM = EPI_SMEM_;
+    // CTAs per cluster along M: the CTAs of a cluster compute vertically adjacent
+    // tiles that share one B tile; each loads 1/CLUSTER of it and multicasts it
+    static constexpr int CLUSTER = CLUSTER_;
     static constexpr int PROMO_WARPS = 8;
     static constexpr int CPW = BN / 2;       // output columns per promotion warp
     static constexpr int THREADS = 128 + 32 * PROMO_WARPS;
     static constexpr bool REG_SPLIT = (BN == 256);
-    static constexpr int TMEM_COLS = 2 * BN;
+    // TMEM accumulator buffers: as many BN-column buffers as the 512 columns hold
+    // (2 at BN = 256, 4 at BN = 128), i.e. that many chunks in flight between the
+    // MMA issuer and the promotion warps
+    static constexpr int NBUF = 512 / BN;
+    static constexpr int TMEM_COLS = 512;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SA_BYTES = BM * 4;
@@ -72,7 +84,7 @@ struct GemmConfig {
     static constexpr uint32_t SC_TX = SA_BYTES + SB_BYTES;
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 64 bf16 (4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
-    static constexpr int STAGE_OUT_BYTES = PROMO_WARPS * (CPW / 64) * BOX_BYTES;
+    static constexpr int STAGE_OUT_BYTES = EPI_SMEM ? PROMO_WARPS * (CPW / 64) * BOX_BYTES : 0;
     // shared-memory layout (offsets from a 1024-byte-aligned base)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -80,10 +92,11 @@ struct GemmConfig {
     static constexpr int OFF_SA = OFF_OUT + STAGE_OUT_BYTES;
     static constexpr int OFF_SB = OFF_SA + SSTAGES * SA_BYTES;
     static constexpr int OFF_BAR = OFF_SB + SSTAGES * SB_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * SSTAGES + 4 + 1;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * SSTAGES + 2 * NBUF + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN == 256), "clusters of 2 with 256-wide tiles only");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     // registers per thread at launch (65536 / 384, rounded down to a multiple of 8)
     static constexpr int LAUNCH_REGS = 168;
@@ -98,24 +111,33 @@ struct GemmArgs {
     int gm, gn, num_chunks;
     int tiles_m, tiles_n;
     int n_fastest;            // tile order: 1 = sweep the N tiles of a row block first
+    uint16_t* d;              // output (BF16) and its row stride in elements, for direct stores
+    int64_t ldd;
     const float* sb_scalar;   // scalar mode: sB(c, j) = sb_scalar[(j/128) * sb_col_stride + c * sb_chunk_stride]
     int64_t sb_col_stride, sb_chunk_stride;
     unsigned* status;
 };
 
+// Origin of the t-th tile of this CTA. Tiles are handed out in a static
+// round-robin over clusters; the CTAs of a cluster take vertically adjacent
+// tiles (same columns) of one "super tile" of CLUSTER x 1 tiles.
 template <class Cfg>
 __device__ __forceinline__ void tile_origin(const GemmArgs& args, int t, int& m0, int& n0)
 {
-    const int id = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
-    int mb, nb;
+    const int nclusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
+    const int cid = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
+    const int rank = static_cast<int>(blockIdx.x) % Cfg::CLUSTER;
+    const int super_m = (args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER;
+    const int id = cid + t * nclusters;
+    int sm, nb;
     if (args.n_fastest) {
         nb = id % args.tiles_n;
-        mb = id / args.tiles_n;
+        sm = id / args.tiles_n;
     } else {
-        mb = id % args.tiles_m;
-        nb = id / args.tiles_m;
+        sm = id % super_m;
+        nb = id / super_m;
     }
-    m0 = mb * Cfg::BM;
+    m0 = (sm * Cfg::CLUSTER + rank) * Cfg::BM;
     n0 = nb * Cfg::BN;
 }
 
@@ -138,30 +160,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t* sfull = empty + Cfg::STAGES;       // scale stage landed (TMA)
     uint64_t* sempty = sfull + Cfg::SSTAGES;     // scale stage consumed (promotion warps)
     uint64_t* tfull = sempty + Cfg::SSTAGES;     // TMEM buffer holds a finished chunk
-    uint64_t* tempty = tfull + 2;                // TMEM buffer read out
-    uint64_t* mma_done = tempty + 2;
+    uint64_t* tempty = tfull + Cfg::NBUF;        // TMEM buffer read out
+    uint64_t* mma_done = tempty + Cfg::NBUF;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nc = args.num_chunks;
-    const int total_tiles = args.tiles_m * args.tiles_n;
-    const int my_tiles = total_tiles > static_cast<int>(blockIdx.x)
-                             ? (total_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                             : 0;
+    // super tiles (CLUSTER x 1 tiles) handed out round-robin over the clusters
+    const int total_tiles = ((args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER) * args.tiles_n;
+    const int nclusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
+    const int cid = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
+    const uint32_t crank = Cfg::CLUSTER > 1 ? cluster_ctarank() : 0u;
+    const int my_tiles = total_tiles > cid ? (total_tiles - 1 - cid) / nclusters + 1 : 0;
     const int my_chunks = my_tiles * nc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], Cfg::CLUSTER);  // one MMA completion per CTA of the cluster
         }
         for (int s = 0; s < Cfg::SSTAGES; ++s) {
             mbar_init(&sfull[s], 1);
             mbar_init(&sempty[s], Cfg::PROMO_WARPS);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < Cfg::NBUF; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], Cfg::PROMO_WARPS);
         }
@@ -175,7 +199,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmSA);
         if (Cfg::SB_VEC)
             tma_prefetch_desc(&tmSB);
-        tma_prefetch_desc(&tmD);
+        if (Cfg::EPI_SMEM)
+            tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
@@ -183,6 +208,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
+    if (Cfg::CLUSTER > 1)
+        cluster_sync();  // every CTA's barriers are initialised before any multicast reaches them
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -204,7 +231,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 mbar_arrive_expect_tx(&full[s], Cfg::OP_TX);
                 tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], c * Cfg::BK, m0);
-                if (Cfg::B_MN) {
+                if (Cfg::CLUSTER > 1) {
+                    // this CTA's share of the B tile goes to every CTA of the cluster
+                    constexpr uint16_t mask = (1u << Cfg::CLUSTER) - 1;
+                    constexpr int part = Cfg::BN / Cfg::CLUSTER;  // B rows (or MN columns) per CTA
+                    if (Cfg::B_MN)
+                        tma_load_2d_multicast(sB + s * Cfg::B_BYTES + crank * part * Cfg::BK, &tmB, &full[s],
+                                              n0 + crank * part, c * Cfg::BK, mask);
+                    else
+                        tma_load_2d_multicast(sB + s * Cfg::B_BYTES + crank * part * Cfg::BK, &tmB, &full[s],
+                                              c * Cfg::BK, n0 + crank * part, mask);
+                } else if (Cfg::B_MN) {
 #pragma unroll
                     for (int a = 0; a < Cfg::BN / 128; ++a)
                         tma_load_2d(sB + s * Cfg::B_BYTES + a * 128 * Cfg::BK, &tmB, &full[s], n0 + a * 128,
@@ -255,8 +292,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int g = 0; g < my_chunks; ++g) {
                 const int s = g % Cfg::STAGES;
                 const uint32_t ph = (g / Cfg::STAGES) & 1;
-                const int b = g & 1;
-                const uint32_t bph = (g >> 1) & 1;
+                const int b = g % Cfg::NBUF;
+                const uint32_t bph = (g / Cfg::NBUF) & 1;
                 if (!mbar_wait(&full[s], ph, abort_flag, args.status))
                     break;
                 if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, args.status))
@@ -268,7 +305,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < Cfg::BK / 32; ++kk)
                     mma_e4m3(d_tmem, ad + (kk * 32) / 16, bd + (kk * kBStep) / 16, idesc, kk > 0 ? 1u : 0u);
-                mma_commit(&empty[s]);
+                if (Cfg::CLUSTER > 1)
+                    mma_commit_multicast(&empty[s], (1u << Cfg::CLUSTER) - 1);  // the stage is free in every CTA
+                else
+                    mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
             }
             // all issued MMAs must be complete before TMEM is released
@@ -322,8 +362,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int g = 0; g < my_chunks; ++g) {
             const int ss = g % Cfg::SSTAGES;
             const uint32_t sph = (g / Cfg::SSTAGES) & 1;
-            const int b = g & 1;
-            const uint32_t bph = (g >> 1) & 1;
+            const int b = g % Cfg::NBUF;
+            const uint32_t bph = (g / Cfg::NBUF) & 1;
             const float sb_c = sb0;
             sb0 = sb1;
             sb1 = next_sb();
@@ -373,31 +413,48 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (++c == nc) {
                 // ------------------------------------------------ BF16 epilogue of tile t
                 const int col0 = n0 + half * CPW;
-                if (lane == 0)
-                    tma_store_wait_read_all();  // this warp's previous stores have left the slab
-                __syncwarp();
+                if constexpr (Cfg::EPI_SMEM) {
+                    if (lane == 0)
+                        tma_store_wait_read_all();  // this warp's previous stores have left the slab
+                    __syncwarp();
 #pragma unroll
-                for (int bx = 0; bx < CPW / 64; ++bx) {
-                    uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
+                    for (int bx = 0; bx < CPW / 64; ++bx) {
+                        uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint64_t* v = acc + bx * 32 + k * 4;
-                        uint4 pk;
-                        pk.x = cvt_bf16x2(v[0]);
-                        pk.y = cvt_bf16x2(v[1]);
-                        pk.z = cvt_bf16x2(v[2]);
-                        pk.w = cvt_bf16x2(v[3]);
-                        *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                        for (int k = 0; k < 8; ++k) {
+                            const uint64_t* v = acc + bx * 32 + k * 4;
+                            uint4 pk;
+                            pk.x = cvt_bf16x2(v[0]);
+                            pk.y = cvt_bf16x2(v[1]);
+                            pk.z = cvt_bf16x2(v[2]);
+                            pk.w = cvt_bf16x2(v[3]);
+                            *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                        }
                     }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                    for (int bx = 0; bx < CPW / 64; ++bx)
-                        if (col0 + bx * 64 < args.gn && m0 + quarter * 32 < args.gm)
-                            tma_store_2d(&tmD, my_out + bx * Cfg::BOX_BYTES, col0 + bx * 64, m0 + quarter * 32);
-                    tma_store_commit();
+                        for (int bx = 0; bx < CPW / 64; ++bx)
+                            if (col0 + bx * 64 < args.gn && m0 + quarter * 32 < args.gm)
+                                tma_store_2d(&tmD, my_out + bx * Cfg::BOX_BYTES, col0 + bx * 64, m0 + quarter * 32);
+                        tma_store_commit();
+                    }
+                } else {
+                    const int grow = m0 + row;
+                    if (grow < args.gm && col0 < args.gn) {
+                        uint16_t* dst = args.d + static_cast<int64_t>(grow) * args.ldd + col0;
+#pragma unroll
+                        for (int k = 0; k < CPW / 8; ++k) {
+                            const uint64_t* v = acc + k * 4;
+                            uint4 pk;
+                            pk.x = cvt_bf16x2(v[0]);
+                            pk.y = cvt_bf16x2(v[1]);
+                            pk.z = cvt_bf16x2(v[2]);
+                            pk.w = cvt_bf16x2(v[3]);
+                            *reinterpret_cast<uint4*>(dst + 8 * k) = pk;
+                        }
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < CPW / 2; ++i)
@@ -407,12 +464,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tile_origin<Cfg>(args, t, m0, n0);
             }
         }
-        if (lane == 0)
+        if (Cfg::EPI_SMEM && lane == 0)
             tma_store_wait_read_all();
     }
 
     tc_fence_before_sync();
     __syncthreads();
+    if (Cfg::CLUSTER > 1)
+        cluster_sync();  // no CTA leaves while a peer may still multicast into it or signal its barriers
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);

@@ -58,195 +58,132 @@ __device__ __forceinline__ TileScale tile_scale(float amax)
     return t;
 }
 
-// RN(x / s) by two Markstein steps.
-__device__ __forceinline__ float quotient(float x, const TileScale& ts)
+// ---------------------------------------------------------------------------
+// Packed form used by the kernels: two values per 64-bit register pair, so the
+// five quotient steps (one product, two Markstein corrections) are five packed
+// FP32 instructions per pair. Inputs are the magnitudes |x| (the sign is put
+// back into the code bytes), and lane i of every operand belongs to value i.
+// ---------------------------------------------------------------------------
+struct PairScale {
+    uint64_t ns;   // {-sp_lo, -sp_hi}
+    uint64_t y;    // {y_lo, y_hi}
+    uint64_t pre;  // {pre_lo, pre_hi}
+    bool scaled;   // some lane has pre != 1
+};
+
+__device__ __forceinline__ PairScale pair_scale(const TileScale& lo, const TileScale& hi)
 {
-    const float a = fabsf(x) * ts.pre;
-    float q = a * ts.y;
-    float r = fmaf(-q, ts.sp, a);
-    q = fmaf(r, ts.y, q);
-    r = fmaf(-q, ts.sp, a);
-    q = fmaf(r, ts.y, q);
-    return copysignf(q, x);
+    PairScale p;
+    p.ns = pack_f32x2(-lo.sp, -hi.sp);
+    p.y = pack_f32x2(lo.y, hi.y);
+    p.pre = pack_f32x2(lo.pre, hi.pre);
+    p.scaled = lo.pre != 1.0f || hi.pre != 1.0f;
+    return p;
 }
 
-// Codes of N values (N a multiple of 4); out[i] packs codes 4i .. 4i+3, first value in the low byte.
-template <int N>
-__device__ __forceinline__ void encode(const float (&x)[N], const TileScale& ts, uint32_t (&out)[N / 4])
+// |values| of a packed BF16 pair as a packed FP32 pair
+__device__ __forceinline__ uint64_t unpack_abs(uint32_t w)
 {
-    float t[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        t[i] = quotient(x[i], ts);
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i)
-        out[i] = cvt_e4m3x2(t[4 * i], t[4 * i + 1]) | (cvt_e4m3x2(t[4 * i + 2], t[4 * i + 3]) << 16);
+    const uint32_t aw = w & 0x7FFF7FFFu;
+    return pack_f32x2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ float amax_word(uint32_t w)
+// RN(a / s) lane-wise for a packed pair of magnitudes
+__device__ __forceinline__ uint64_t quotient2(uint64_t a, const PairScale& ps)
 {
-    return fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w)));
+    if (ps.scaled)
+        a = fmul2(a, ps.pre);
+    uint64_t q = fmul2(a, ps.y);
+    uint64_t r = a;
+    ffma2(r, q, ps.ns);  // r = a - q s
+    ffma2(q, r, ps.y);   // q = q + r y
+    r = a;
+    ffma2(r, q, ps.ns);
+    ffma2(q, r, ps.y);
+    return q;
 }
 
-__device__ __forceinline__ float amax_v4(const uint4& v)
+// E4M3 codes of a packed FP32 pair (non-negative): low value in bits 0-7
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint64_t q)
 {
-    return fmaxf(fmaxf(amax_word(v.x), amax_word(v.y)), fmaxf(amax_word(v.z), amax_word(v.w)));
+    uint16_t r;
+    asm("{\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 %0, hi, lo;\n\t}"
+        : "=h"(r)
+        : "l"(q));
+    return r;
 }
 
-// 8 BF16 values -> 8 codes (one 64-bit word, first value in the low byte).
-__device__ __forceinline__ uint2 codes8(const uint4& v, const TileScale& ts)
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
-    const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                        bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-    uint32_t o[2];
-    encode<8>(x, ts, o);
-    return make_uint2(o[0], o[1]);
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// amax over the 16 lanes that share one 1x128 tile (lanes 0-15 or 16-31).
-__device__ __forceinline__ float amax16(float a)
+// lane-wise max of |values| over the 4 BF16 pairs of a 16-byte vector
+__device__ __forceinline__ uint32_t absmax_pairs(const uint4& v)
 {
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    return a;
+    return bf16x2_max(bf16x2_max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                      bf16x2_max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+}
+
+// 8 BF16 values sharing one tile scale -> 8 codes (first value in the low byte)
+__device__ __forceinline__ uint2 codes8_packed(const uint4& v, const PairScale& ps)
+{
+    const uint32_t c0 = cvt_e4m3x2(quotient2(unpack_abs(v.x), ps));
+    const uint32_t c1 = cvt_e4m3x2(quotient2(unpack_abs(v.y), ps));
+    const uint32_t c2 = cvt_e4m3x2(quotient2(unpack_abs(v.z), ps));
+    const uint32_t c3 = cvt_e4m3x2(quotient2(unpack_abs(v.w), ps));
+    // sign bits: bit 7 of bytes 1 and 3 of each BF16 pair word
+    const uint32_t s01 = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
+    const uint32_t s23 = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
+    return make_uint2((c0 | (c1 << 16)) | s01, (c2 | (c3 << 16)) | s23);
 }
 
 // ---------------------------------------------------------------------------
-// 1x128 activation tiles along the columns of x [R][C] (C a multiple of 128).
-// 16 threads own one tile (8 values each); a warp covers two neighbouring
-// tiles, i.e. 512 contiguous bytes of a row. Each thread handles UNROLL tiles
-// (all loads issued first for memory-level parallelism).
-// q [R][C] (ldq), s [C/128][R] (lds).
+// Column pass (transposed tiles). The 128x128 BF16 block sits row-major in
+// shared memory (rows past R hold +0). Warp w takes rows 32 (w%4) .. +31 of
+// the column pair 64 (w/4) + 2 lane, +1 (conflict-free 4-byte reads, one BF16
+// pair per read: the two columns travel as the two lanes of every packed
+// operation, each with its own scale); the four row quarters combine their
+// amax through shared memory. Codes go to qt [C][R128] (row = input column),
+// scales to st [R128/128][C]. Pad rows hold +0 and so get code 0x00.
 // ---------------------------------------------------------------------------
-template <int UNROLL>
-__global__ void __launch_bounds__(256) quant_act_kernel(const uint16_t* __restrict__ x, int64_t ldx,
-                                                        uint8_t* __restrict__ q, int64_t ldq,
-                                                        float* __restrict__ s, int64_t lds,
-                                                        int64_t nchunks, int64_t ntiles)
-{
-    const int sub = threadIdx.x & 15;
-    const int64_t first = (int64_t)blockIdx.x * (16 * UNROLL) + (threadIdx.x >> 4);
-    uint4 v[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-        const int64_t t = first + u * 16;
-        if (t < ntiles) {
-            const int64_t r = t / nchunks, c = t - r * nchunks;
-            v[u] = ld_stream_v4(x + r * ldx + c * 128 + sub * 8);
-        } else {
-            v[u] = make_uint4(0, 0, 0, 0);
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-        const float a = amax16(amax_v4(v[u]));
-        const int64_t t = first + u * 16;
-        if (t < ntiles) {
-            const int64_t r = t / nchunks, c = t - r * nchunks;
-            const TileScale ts = tile_scale(a);
-            *reinterpret_cast<uint2*>(q + r * ldq + c * 128 + sub * 8) = codes8(v[u], ts);
-            if (sub == 0)
-                s[c * lds + r] = ts.s;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// 128x128 weight blocks: one CTA (256 threads) per block. Thread t reads 8
-// values of column group t%16 in rows t/16 + 16 i (i < 8); the block amax is
-// reduced with shuffles and then across the 8 warps in shared memory.
-// q [N][K] (ldq), s [N/128][K/128] dense.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_weight_kernel(const uint16_t* __restrict__ w, int64_t ldw,
-                                                           uint8_t* __restrict__ q, int64_t ldq,
-                                                           float* __restrict__ s, int64_t kblocks)
-{
-    __shared__ float red[8];
-    const int tid = threadIdx.x;
-    const int cg = tid & 15, r0 = tid >> 4;
-    const int64_t bi = blockIdx.y, bj = blockIdx.x;
-    const uint16_t* base = w + (bi * 128 + r0) * ldw + bj * 128 + cg * 8;
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        v[i] = ld_stream_v4(base + (int64_t)(16 * i) * ldw);
-    float a = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        a = fmaxf(a, amax_v4(v[i]));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-    if ((tid & 31) == 0)
-        red[tid >> 5] = a;
-    __syncthreads();
-    a = red[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i)
-        a = fmaxf(a, red[i]);
-    const TileScale ts = tile_scale(a);
-    uint8_t* qb = q + (bi * 128 + r0) * ldq + bj * 128 + cg * 8;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<uint2*>(qb + (int64_t)(16 * i) * ldq) = codes8(v[i], ts);
-    if (tid == 0)
-        s[bi * kblocks + bj] = ts.s;
-}
-
-// ---------------------------------------------------------------------------
-// Column pass shared by the transposed and the dual kernel. The 128x128 BF16
-// block sits row-major in shared memory (rows past R hold +0). Warp w takes
-// rows 32 (w%4) .. +31 of the column pair 64 (w/4) + 2 lane, +1 (conflict-free
-// 4-byte reads); the four row quarters combine their amax through shared
-// memory. Codes go to qt [C][R128] (row = input column), scales to
-// st [R128/128][C]. Pad rows hold +0 and so get code 0x00.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], float (*part)[128], int64_t cb, int64_t rb,
+__device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t (*part)[64], int64_t cb, int64_t rb,
                                             uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ st,
                                             int64_t ldst)
 {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;
-    const int col = (warp >> 2) * 64 + 2 * lane;  // first of the thread's two columns
-    float a0 = 0.0f, a1 = 0.0f;
+    const int cw = (warp >> 2) * 32 + lane;  // the thread's column pair (word index in a row)
+    const int col = 2 * cw;                  // first of the thread's two columns
+    // lane-wise |max| of the pair over this quarter's 32 rows, combined across quarters
+    uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t w = tile[quarter * 32 + i][col >> 1];
-        a0 = fmaxf(a0, fabsf(bf16_lo(w)));
-        a1 = fmaxf(a1, fabsf(bf16_hi(w)));
-    }
-    *reinterpret_cast<float2*>(&part[quarter][col]) = make_float2(a0, a1);
+    for (int i = 0; i < 32; ++i)
+        m = bf16x2_max(m, tile[quarter * 32 + i][cw] & 0x7FFF7FFFu);
+    part[quarter][cw] = m;
     __syncthreads();
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const float2 p = *reinterpret_cast<const float2*>(&part[qq][col]);
-        a0 = fmaxf(a0, p.x);
-        a1 = fmaxf(a1, p.y);
-    }
-    const TileScale s0 = tile_scale(a0), s1 = tile_scale(a1);
+    m = bf16x2_max(bf16x2_max(part[0][cw], part[1][cw]), bf16x2_max(part[2][cw], part[3][cw]));
+    const TileScale s0 = tile_scale(bf16_lo(m)), s1 = tile_scale(bf16_hi(m));
+    const PairScale ps = pair_scale(s0, s1);
 
-    // column col: low halves; column col+1: high halves. 32 rows -> 32 codes each,
-    // re-read from shared memory and encoded 8 at a time to bound register use.
+    // rows in groups of 4: each row's pair gives code(col) in byte 0, code(col+1) in byte 1
     uint32_t c0[8], c1[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float x0[8], x1[8];
+    for (int j = 0; j < 8; ++j) {
+        uint32_t c[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w = tile[quarter * 32 + 8 * j + i][col >> 1];
-            x0[i] = bf16_lo(w);
-            x1[i] = bf16_hi(w);
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t w = tile[quarter * 32 + 4 * j + i][cw];
+            c[i] = cvt_e4m3x2(quotient2(unpack_abs(w), ps)) | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
         }
-        uint32_t o0[2], o1[2];
-        encode<8>(x0, s0, o0);
-        encode<8>(x1, s1, o1);
-        c0[2 * j] = o0[0];
-        c0[2 * j + 1] = o0[1];
-        c1[2 * j] = o1[0];
-        c1[2 * j + 1] = o1[1];
+        const uint32_t a = c[0] | (c[1] << 16), b = c[2] | (c[3] << 16);
+        c0[j] = __byte_perm(a, b, 0x6420);
+        c1[j] = __byte_perm(a, b, 0x7531);
     }
     uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + quarter * 32;
     uint8_t* out1 = out0 + ldqt;
@@ -259,88 +196,142 @@ __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], float (*
 }
 
 // ---------------------------------------------------------------------------
-// Transposed 1x128 tiles: tiles run down the columns of x [R][C] (along R, the
-// contraction axis of the weight-gradient GEMM); codes are written transposed,
-// qt [C][R128] (ldqt), scales st [R128/128][C] (ldst). One CTA per 128x128
-// input block: the block is staged row-major in shared memory (coalesced
-// 16-byte loads, zero rows past R), then the column pass.
+// Persistent, TMA-fed quantiser over 128x128 blocks of a BF16 matrix x [R][C]
+// (C a multiple of 128; rows past R read as +0 through the tensor map). Each
+// CTA walks the blocks blockIdx.x, blockIdx.x + gridDim.x, ...; one thread
+// keeps two blocks in flight (double-buffered 32 KB shared-memory tiles filled
+// by cp.async.bulk.tensor, completion on an mbarrier) while all 256 threads
+// encode the current one, so HBM reads overlap the arithmetic.
+//   MODE_ROWS:   1x128 tiles along the columns -> q [R][C], s [C/128][R]
+//   MODE_COLS:   1x128 tiles down the rows     -> qt [C][R128], st [R128/128][C]
+//   MODE_DUAL:   both of the above from one read of x
+//   MODE_WEIGHT: one 128x128 block per scale   -> q [R][C], s [R/128][C/128]
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256, 3) quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t R,
-                                                              int64_t ldx, uint8_t* __restrict__ qt,
-                                                              int64_t ldqt, float* __restrict__ st,
-                                                              int64_t ldst)
-{
-    __shared__ __align__(16) uint32_t tile[128][64];  // 128 rows x 128 bf16
-    __shared__ __align__(16) float part[4][128];
-    const int tid = threadIdx.x;
-    const int64_t cb = blockIdx.x, rb = blockIdx.y;
+enum QuantMode { MODE_ROWS = 1, MODE_COLS = 2, MODE_DUAL = 3, MODE_WEIGHT = 4 };
 
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = tid + 256 * i;
-        const int row = idx >> 4, cv = idx & 15;
-        const int64_t gr = rb * 128 + row;
-        v[i] = (gr < R) ? ld_stream_v4(x + gr * ldx + cb * 128 + cv * 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = tid + 256 * i;
-        *reinterpret_cast<uint4*>(&tile[idx >> 4][(idx & 15) * 4]) = v[i];
-    }
-    __syncthreads();
-    column_pass(tile, part, cb, rb, qt, ldqt, st, ldst);
-}
+struct QuantArgs {
+    int64_t R, nblk_c, nblocks;
+    uint8_t* q;
+    int64_t ldq;
+    float* s;
+    int64_t lds;
+    uint8_t* qt;
+    int64_t ldqt;
+    float* st;
+    int64_t ldst;
+    unsigned* status;
+};
 
-// ---------------------------------------------------------------------------
-// Both layouts of one activation in a single pass over HBM: the 1x128 tiles
-// along the columns (q [R][C], s [C/128][R], as quant_act_kernel) and the
-// transposed tiles along the rows (qt [C][R128], st [R128/128][C], as
-// quant_transpose_kernel). One CTA per 128x128 block; thread t's i-th 16-byte
-// load holds 8 values of row t/16 + 16 i, so the 16 lanes of a half-warp own
-// one 1x128 row tile and reduce its amax with shuffles while the block is
-// staged in shared memory for the column pass.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256, 3) quant_dual_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t ldx,
-                                                         uint8_t* __restrict__ q, int64_t ldq,
-                                                         float* __restrict__ s, int64_t lds,
-                                                         uint8_t* __restrict__ qt, int64_t ldqt,
-                                                         float* __restrict__ st, int64_t ldst)
+constexpr int kQuantTileBytes = 128 * 128 * 2;
+constexpr int kQuantSmemBytes = 2 * kQuantTileBytes + 1024;  // two tiles + alignment slack
+
+template <int MODE>
+__global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_constant__ CUtensorMap tmX, const QuantArgs a)
 {
-    __shared__ __align__(16) uint32_t tile[128][64];
-    __shared__ __align__(16) float part[4][128];
+    extern __shared__ uint8_t qsmem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(16) uint32_t part[4][64];
+    __shared__ uint32_t red[8];
+    __shared__ int abort_flag;
     const int tid = threadIdx.x;
     const int sub = tid & 15;
-    const int64_t cb = blockIdx.x, rb = blockIdx.y;
 
-    uint4 v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = tid + 256 * i;
-        const int row = idx >> 4;
-        const int64_t gr = rb * 128 + row;
-        v[i] = (gr < R) ? ld_stream_v4(x + gr * ldx + cb * 128 + sub * 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = tid + 256 * i;
-        *reinterpret_cast<uint4*>(&tile[idx >> 4][sub * 4]) = v[i];
-    }
-    // row tiles (1x128 along the columns) from the registers
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = (tid >> 4) + 16 * i;
-        const int64_t gr = rb * 128 + row;
-        const float a = amax16(amax_v4(v[i]));
-        if (gr < R) {
-            const TileScale ts = tile_scale(a);
-            *reinterpret_cast<uint2*>(q + gr * ldq + cb * 128 + sub * 8) = codes8(v[i], ts);
-            if (sub == 0)
-                s[cb * lds + gr] = ts.s;
-        }
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int my_blocks = a.nblocks > first ? static_cast<int>((a.nblocks - 1 - first) / stride + 1) : 0;
+
+    auto issue = [&](int i) {  // thread 0: load my i-th block into buffer i & 1
+        const int64_t b = first + static_cast<int64_t>(i) * stride;
+        const int64_t rb = b / a.nblk_c, cb = b - rb * a.nblk_c;
+        uint64_t* bar = &full[i & 1];
+        mbar_arrive_expect_tx(bar, kQuantTileBytes);
+        tma_load_2d(tiles + (i & 1) * kQuantTileBytes, &tmX, bar, static_cast<int32_t>(cb * 128),
+                    static_cast<int32_t>(rb * 128));
+    };
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tmX);
     }
     __syncthreads();
-    column_pass(tile, part, cb, rb, qt, ldqt, st, ldst);
+    if (tid == 0) {
+        if (my_blocks > 0)
+            issue(0);
+        if (my_blocks > 1)
+            issue(1);
+    }
+
+    int i = 0;
+    for (; i < my_blocks; ++i) {
+        const int64_t b = first + static_cast<int64_t>(i) * stride;
+        const int64_t rb = b / a.nblk_c, cb = b - rb * a.nblk_c;
+        // every thread takes the same decision, so no thread can be left at a barrier
+        if (!__syncthreads_and(mbar_wait(&full[i & 1], (i >> 1) & 1, &abort_flag, a.status)))
+            break;
+        const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + (i & 1) * kQuantTileBytes);
+
+        if (MODE == MODE_ROWS || MODE == MODE_DUAL) {
+            // thread t: rows t/16 + 16 j, columns 8 (t%16) .. +7; a half-warp owns one row tile
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                const int row = (tid >> 4) + 16 * j;
+                const int64_t gr = rb * 128 + row;
+                const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
+                uint32_t m = absmax_pairs(v);
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                if (gr < a.R) {
+                    const TileScale ts = tile_scale(fmaxf(bf16_lo(m), bf16_hi(m)));
+                    *reinterpret_cast<uint2*>(a.q + gr * a.ldq + cb * 128 + sub * 8) =
+                        codes8_packed(v, pair_scale(ts, ts));
+                    if (sub == 0)
+                        a.s[cb * a.lds + gr] = ts.s;
+                }
+            }
+        }
+        if (MODE == MODE_COLS || MODE == MODE_DUAL)
+            column_pass(tile, part, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+        if (MODE == MODE_WEIGHT) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                m = bf16x2_max(m, absmax_pairs(*reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4])));
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if ((tid & 31) == 0)
+                red[tid >> 5] = m;
+            __syncthreads();
+            m = red[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+                m = bf16x2_max(m, red[k]);
+            const TileScale ts = tile_scale(fmaxf(bf16_lo(m), bf16_hi(m)));
+            const PairScale ps = pair_scale(ts, ts);
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                const int row = (tid >> 4) + 16 * j;
+                const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
+                *reinterpret_cast<uint2*>(a.q + (rb * 128 + row) * a.ldq + cb * 128 + sub * 8) = codes8_packed(v, ps);
+            }
+            if (tid == 0)
+                a.s[rb * a.lds + cb] = ts.s;
+        }
+        __syncthreads();  // everyone is done with this buffer (and with part / red)
+        if (tid == 0 && i + 2 < my_blocks)
+            issue(i + 2);
+    }
+    // an aborted CTA must not exit while a copy may still land in its shared memory
+    if (tid == 0 && i < my_blocks) {
+        volatile int never = 0;
+        for (int k = i; k < my_blocks && k < i + 2; ++k)
+            mbar_wait(&full[k & 1], (k >> 1) & 1, &never, a.status);
+    }
 }
 
 }  // namespace bfp8

@@ -1,7 +1,9 @@
 // Exhaustive check of the quantisers' division-free quotient (quant.cuh) against
 // the IEEE binary32 division, over the whole input domain the kernels can see:
 // every finite BF16 tile maximum `amax` >= 0 (s = RN(amax/448)) and every finite
-// BF16 value x with |x| <= amax. Two counts, both must be zero:
+// BF16 value x with |x| <= amax, each in the low lane of a packed pair (with
+// another admissible value in the high lane, checked as well), exactly as the
+// kernels compute it. Two counts, both must be zero:
 //   code mismatches: E4M3 code of the quotient differs from that of x / s;
 //   quotient mismatches: the quotient's bits differ from x / s, counted where
 //     |x / s| >= 2^-12 (below 2^-10 every code is a signed zero).
@@ -17,22 +19,35 @@ __global__ void check(unsigned long long* pairs, unsigned long long* bad, unsign
     const unsigned ab = blockIdx.y;  // amax bit pattern (0 .. largest finite)
     const float amax = __uint_as_float(ab << 16);
     const bfp8::TileScale ts = bfp8::tile_scale(amax);
+    const bfp8::PairScale ps = bfp8::pair_scale(ts, ts);
     unsigned long long n = 0;
     for (unsigned xb = blockIdx.x * blockDim.x + threadIdx.x; xb < 65536u; xb += gridDim.x * blockDim.x) {
         if ((xb & 0x7FFFu) > ab)
             continue;  // |x| > amax never occurs in a tile
-        const float x = __uint_as_float(xb << 16);
-        const float q = bfp8::quotient(x, ts);
-        const float d = ts.s == 0.0f ? x : __fdiv_rn(x, ts.s);
-        ++n;
-        const bool code_differs = bfp8::cvt_e4m3x2(q, 0.0f) != bfp8::cvt_e4m3x2(d, 0.0f);
-        const bool quot_differs = fabsf(d) >= 0x1p-12f && __float_as_uint(q) != __float_as_uint(d);
-        if (code_differs || quot_differs) {
-            const unsigned long long k = atomicAdd(bad, 1ull);
-            if (k < 4) {
-                first[3 * k] = xb;
-                first[3 * k + 1] = ab;
-                first[3 * k + 2] = __float_as_uint(q);
+        // the value travels in the low lane; a second value (any other admissible one) in the high lane
+        unsigned xb2 = (xb * 40503u + 7u) & 0xFFFFu;
+        if ((xb2 & 0x7FFFu) > ab)
+            xb2 &= 0x8000u;
+        const uint32_t w = xb | (xb2 << 16);
+        const uint64_t q = bfp8::quotient2(bfp8::unpack_abs(w), ps);
+        const uint32_t code = bfp8::cvt_e4m3x2(q) | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
+        const unsigned vals[2] = {xb, xb2};
+#pragma unroll
+        for (int lane = 0; lane < 2; ++lane) {
+            const float x = __uint_as_float(vals[lane] << 16);
+            const float ql = __uint_as_float(static_cast<uint32_t>(q >> (32 * lane)));  // |x| / s
+            const float d = ts.s == 0.0f ? x : __fdiv_rn(x, ts.s);                    // the definition
+            ++n;
+            const uint32_t want = bfp8::cvt_e4m3x2(d, 0.0f) & 0xFFu;
+            const bool code_differs = ((code >> (8 * lane)) & 0xFFu) != want;
+            const bool quot_differs = fabsf(d) >= 0x1p-12f && __float_as_uint(ql) != __float_as_uint(fabsf(d));
+            if (code_differs || quot_differs) {
+                const unsigned long long k = atomicAdd(bad, 1ull);
+                if (k < 4) {
+                    first[3 * k] = vals[lane];
+                    first[3 * k + 1] = ab;
+                    first[3 * k + 2] = __float_as_uint(ql);
+                }
             }
         }
     }

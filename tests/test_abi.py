@@ -23,7 +23,8 @@ def test_exports_every_declared_function(lib):
     assert set(names) >= {"fp8_quantize_act", "fp8_quantize_weight", "fp8_quantize_transpose",
                           "fp8_quantize_act_transpose",
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
-                          "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n"}
+                          "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
+                          "bfp8_set_gemm_cluster"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
         assert hasattr(cdll, n), n
@@ -39,6 +40,9 @@ def test_tile_knob(lib):
     assert lib.bfp8_set_gemm_tile_n(64) == EINVAL
     prev = lib.bfp8_set_gemm_tile_n(256)
     assert lib.bfp8_set_gemm_tile_n(prev) == 256
+    assert lib.bfp8_set_gemm_cluster(3) == EINVAL
+    prev = lib.bfp8_set_gemm_cluster(1)
+    assert lib.bfp8_set_gemm_cluster(prev) == 1
 
 
 def test_quantiser_argument_checks(lib):

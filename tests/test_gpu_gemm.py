@@ -22,11 +22,16 @@ pytestmark = pytest.mark.gpu
 TILE = 128
 
 
-@pytest.fixture(params=[128, 256], ids=lambda t: f"tileN{t}")
+@pytest.fixture(params=[(128, 1), (256, 1), (256, 2)], ids=lambda p: f"tileN{p[0]}-cluster{p[1]}")
 def tile_n(request):
-    prev = bfp8.set_gemm_tile_n(request.param)
-    yield request.param
-    bfp8.set_gemm_tile_n(prev)
+    """Every tile configuration: 128-wide tiles, 256-wide tiles one CTA each, and
+    256-wide tiles in clusters of two CTAs sharing B through multicast."""
+    tn, cl = request.param
+    prev_t = bfp8.set_gemm_tile_n(tn)
+    prev_c = bfp8.set_gemm_cluster(cl)
+    yield tn
+    bfp8.set_gemm_tile_n(prev_t)
+    bfp8.set_gemm_cluster(prev_c)
 
 
 def _check(y_gpu, y_ref, what):
