@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 256], help="GEMM tile width (0: automatic)")
     p.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2], help="GEMM CTAs per cluster (0: automatic)")
+    p.add_argument("--gemm-promo-warps", type=int, default=0, choices=[0, 8, 16],
+                   help="GEMM promotion warps per CTA (0: library default)")
     return p.parse_args()
 
 
@@ -244,6 +246,8 @@ def run_ours(args):
     bfp8.load_library()
     bfp8.set_gemm_tile_n(args.gemm_tile_n)
     bfp8.set_gemm_cluster(args.gemm_cluster)
+    if args.gemm_promo_warps:
+        bfp8.set_gemm_promo_warps(args.gemm_promo_warps)
 
     work = workload(args.workload)
     dev = torch.device("cuda", local)
@@ -362,46 +366,76 @@ def run_ours(args):
                                 f"{peak_src}: hbm_gbs ({hbm_peak})")}
 
     # ------------------------------------------------------------ end to end (host buffers)
+    # Every step copies x, W and dy of every linear in from pinned host memory and
+    # y, dx and dW out, through the public API. Copies in, compute and copies out
+    # run on three streams ordered by events, with two buffer sets per linear, so
+    # the copies of one linear overlap the kernels of another.
     e2e = None
     if not args.no_e2e:
-        dev_in = [tuple(torch.empty_like(t, device=dev) for t in h) for h in host]
+        sets = [[(tuple(torch.empty_like(t, device=dev) for t in h),
+                  bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev) if k else L)
+                 for h, lin, L in zip(host, work.linears, layers)] for k in range(2)]
         outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.y, L.dx, L.dw))
                      for L in layers]
         bi = sum(t.numel() * 2 for h in host for t in h)
         bo = sum(t.numel() * 2 for L in layers for t in ((L.y,) if fwd_only else (L.y, L.dx, L.dw)))
         e2e_steps = max(3, min(args.steps, 50))
+        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        nl = len(layers)
+        ev_in = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+        ev_cmp = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+        ev_out = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+        started = [[False] * nl for _ in range(2)]
 
-        def e2e_step():
-            for L, h, d, o in zip(layers, host, dev_in, outs_host):
-                for src, dst in zip(h, d):
-                    dst.copy_(src, non_blocking=True)
-                if fwd_only:
-                    bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
-                    bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
-                    bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
-                else:
-                    L.forward(d[0], d[1])
-                o[0].copy_(L.y, non_blocking=True)
-                if not fwd_only:
-                    L.backward(d[2])
-                    o[1].copy_(L.dx, non_blocking=True)
-                    o[2].copy_(L.dw, non_blocking=True)
+        def e2e_step(k):
+            p = k & 1
+            for i, (h, o) in enumerate(zip(host, outs_host)):
+                d, L = sets[p][i]
+                with torch.cuda.stream(s_in):
+                    if started[p][i]:
+                        s_in.wait_event(ev_cmp[p][i])  # the previous use of this input set is done
+                    for src, dst in zip(h, d):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[p][i].record(s_in)
+                with torch.cuda.stream(s_cmp):
+                    s_cmp.wait_event(ev_in[p][i])
+                    if started[p][i]:
+                        s_cmp.wait_event(ev_out[p][i])  # its outputs have been copied out
+                    if fwd_only:
+                        bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
+                        bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
+                        bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+                    else:
+                        L.forward(d[0], d[1])
+                        L.backward(d[2])
+                    ev_cmp[p][i].record(s_cmp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_cmp[p][i])
+                    o[0].copy_(L.y, non_blocking=True)
+                    if not fwd_only:
+                        o[1].copy_(L.dx, non_blocking=True)
+                        o[2].copy_(L.dw, non_blocking=True)
+                    ev_out[p][i].record(s_out)
+                started[p][i] = True
 
-        for _ in range(2):
-            e2e_step()
+        for k in range(2):
+            e2e_step(k)
         torch.cuda.synchronize()
         barrier(ws)
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        s1.record(stream)
+        s0.record(s_in)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_cmp)
+        s1.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = allreduce_max(s0.elapsed_time(s1), ws, dev)
         e2e = {"value": round(work.flops * e2e_steps * ws / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
-               "how": "pinned host x, W, dy copied in and y, dx, dW copied out every step, same stream"}
+               "how": ("pinned host x, W, dy copied in and y, dx, dW copied out every step; copies in, "
+                       "compute and copies out on three streams ordered by events, two buffer sets per linear")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -66,6 +66,7 @@ def load_library(path: str = LIB_PATH):
         "bfp8_last_device_status": [p],
         "bfp8_set_gemm_tile_n": [c_int],
         "bfp8_set_gemm_cluster": [c_int],
+        "bfp8_set_gemm_promo_warps": [c_int],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -232,6 +233,14 @@ def set_gemm_cluster(cluster: int) -> int:
     rc = load_library().bfp8_set_gemm_cluster(int(cluster))
     if rc < 0:
         raise ValueError("cluster must be 0, 1 or 2")
+    return rc
+
+
+def set_gemm_promo_warps(warps: int) -> int:
+    """Promotion warps per CTA for 256-wide GEMM tiles: 8 or 16. Returns the previous value."""
+    rc = load_library().bfp8_set_gemm_promo_warps(int(warps))
+    if rc < 0:
+        raise ValueError("warps must be 8 or 16")
     return rc
 
 

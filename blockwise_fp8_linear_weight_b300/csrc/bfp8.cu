@@ -28,6 +28,7 @@ constexpr int64_t kMaxGridY = 65535;
 
 std::atomic<int> g_tile_n{0};
 std::atomic<int> g_cluster{0};
+std::atomic<int> g_promo_warps{8};
 
 // ----------------------------------------------------------------- helpers
 bool aligned(const void* p, uintptr_t a)
@@ -267,6 +268,8 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
         cl = 1;  // measured: multicast halves L2 traffic but the path is not L2-bound
     if (cl == 2)
         return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 2>>(p, status, stream, dev);
+    if (g_promo_warps.load(std::memory_order_relaxed) == 16)
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1, true, 16>>(p, status, stream, dev);
     return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1>>(p, status, stream, dev);
 }
 
@@ -567,6 +570,13 @@ extern "C" int bfp8_last_device_status(void* stream)
         cudaStreamSynchronize(st) != cudaSuccess)
         return BFP8_ELAUNCH;
     return (host & kDevTimeout) ? BFP8_ETIMEOUT : BFP8_OK;
+}
+
+extern "C" int bfp8_set_gemm_promo_warps(int warps)
+{
+    if (warps != 8 && warps != 16)
+        return BFP8_EINVAL;
+    return g_promo_warps.exchange(warps);
 }
 
 extern "C" int bfp8_set_gemm_cluster(int cluster)

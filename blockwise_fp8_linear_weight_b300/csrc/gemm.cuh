@@ -50,7 +50,7 @@
 
 namespace bfp8 {
 
-template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, bool EPI_SMEM_ = true>
+template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, bool EPI_SMEM_ = true, int PW_ = 8>
 struct GemmConfig {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -67,8 +67,12 @@ struct GemmConfig {
     // CTAs per cluster along M: the CTAs of a cluster compute vertically adjacent
     // tiles that share one B tile; each loads 1/CLUSTER of it and multicasts it
     static constexpr int CLUSTER = CLUSTER_;
-    static constexpr int PROMO_WARPS = 8;
-    static constexpr int CPW = BN / 2;       // output columns per promotion warp
+    // Promotion warps: PW/4 column groups per TMEM lane quarter. More warps hide the
+    // TMEM-load latency behind other warps' arithmetic; fewer leave more registers.
+    static constexpr int PROMO_WARPS = PW_;
+    static constexpr int GROUPS = PW_ / 4;
+    static constexpr int CPW = BN / GROUPS;  // output columns per promotion warp
+    static constexpr int LW = CPW == 64 && PW_ == 16 ? 32 : 64;  // columns per TMEM load
     static constexpr int THREADS = 128 + 32 * PROMO_WARPS;
     static constexpr bool REG_SPLIT = (BN == 256);
     // TMEM accumulator buffers: as many BN-column buffers as the 512 columns hold
@@ -98,13 +102,14 @@ struct GemmConfig {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN == 256), "clusters of 2 with 256-wide tiles only");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    // registers per thread at launch (65536 / 384, rounded down to a multiple of 8)
-    static constexpr int LAUNCH_REGS = 168;
+    // registers per thread at launch (65536 / THREADS, rounded down to a multiple of 8)
+    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
     // setmaxnreg split between the producer/MMA warpgroup and the two promotion
     // warpgroups (chosen so that neither side spills on its hot path)
-    static constexpr int REG_LOW = SB_VEC ? 64 : 56;
-    static constexpr int REG_HIGH = SB_VEC ? 216 : 224;
-    static_assert(!REG_SPLIT || 128 * REG_LOW + 256 * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
+    static constexpr int REG_LOW = PW_ == 16 ? 32 : (SB_VEC ? 64 : 56);
+    static constexpr int REG_HIGH = PW_ == 16 ? 112 : (SB_VEC ? 216 : 224);
+    static_assert(PW_ == 8 || PW_ == 16, "8 or 16 promotion warps");
+    static_assert(!REG_SPLIT || 128 * REG_LOW + 32 * PW_ * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
 };
 
 struct GemmArgs {
@@ -283,33 +288,53 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(Cfg::BM, Cfg::BN, Cfg::B_MN);
             // Descriptors of stage 0, K step 0; the others differ only in the start
-            // address field (bits 0-13, in 16-byte units), which never carries over
-            // because shared-memory addresses stay below 256 KB.
+            // address field (bits 0-13 of the low word, in 16-byte units), which never
+            // carries over because shared-memory addresses stay below 256 KB. The loop
+            // keeps its ring positions as counters, so it issues no integer multiply
+            // or division: this thread shares its SM sub-partition with promotion
+            // warps whose packed FMAs keep the FMA pipe busy.
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const uint64_t b_desc0 = Cfg::B_MN ? smem_desc_sw128(smem_u32(sB), 128 * Cfg::BK, 1024)
                                                : smem_desc_sw128(smem_u32(sB), 16, 1024);
-            constexpr uint32_t kBStep = Cfg::B_MN ? 32 * 128 : 32;  // bytes per K step of 32
+            const uint32_t a_lo = static_cast<uint32_t>(a_desc0), a_hi = static_cast<uint32_t>(a_desc0 >> 32);
+            const uint32_t b_lo = static_cast<uint32_t>(b_desc0), b_hi = static_cast<uint32_t>(b_desc0 >> 32);
+            constexpr uint32_t kBStep = (Cfg::B_MN ? 32 * 128 : 32) / 16;  // 16-byte units per K step of 32
+            int s = 0, b = 0;
+            uint32_t ph = 0, bph = 0, a_off = 0, b_off = 0, d_tmem = tmem_base;
             for (int g = 0; g < my_chunks; ++g) {
-                const int s = g % Cfg::STAGES;
-                const uint32_t ph = (g / Cfg::STAGES) & 1;
-                const int b = g % Cfg::NBUF;
-                const uint32_t bph = (g / Cfg::NBUF) & 1;
                 if (!mbar_wait(&full[s], ph, abort_flag, args.status))
                     break;
                 if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, args.status))
                     break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + b * Cfg::BN;
-                const uint64_t ad = a_desc0 + static_cast<uint64_t>((s * Cfg::A_BYTES) >> 4);
-                const uint64_t bd = b_desc0 + static_cast<uint64_t>((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < Cfg::BK / 32; ++kk)
-                    mma_e4m3(d_tmem, ad + (kk * 32) / 16, bd + (kk * kBStep) / 16, idesc, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < Cfg::BK / 32; ++kk) {
+                    uint64_t ad, bd;
+                    asm("mov.b64 %0, {%1, %2};" : "=l"(ad) : "r"(a_lo + a_off + kk * 2), "r"(a_hi));
+                    asm("mov.b64 %0, {%1, %2};" : "=l"(bd) : "r"(b_lo + b_off + kk * kBStep), "r"(b_hi));
+                    mma_e4m3(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
                 if (Cfg::CLUSTER > 1)
                     mma_commit_multicast(&empty[s], (1u << Cfg::CLUSTER) - 1);  // the stage is free in every CTA
                 else
                     mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
+                if (++s == Cfg::STAGES) {
+                    s = 0;
+                    ph ^= 1;
+                    a_off = 0;
+                    b_off = 0;
+                } else {
+                    a_off += Cfg::A_BYTES / 16;
+                    b_off += Cfg::B_BYTES / 16;
+                }
+                if (++b == Cfg::NBUF) {
+                    b = 0;
+                    bph ^= 1;
+                    d_tmem = tmem_base;
+                } else {
+                    d_tmem += Cfg::BN;
+                }
             }
             // all issued MMAs must be complete before TMEM is released
             mma_commit(mma_done);
@@ -322,8 +347,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REG_HIGH));
         // ---------------------------------------------------------------- promotion + epilogue
         constexpr int CPW = Cfg::CPW;
-        const int pw = warp - 4;            // 0 .. 7
-        const int half = pw >> 2;           // which half of the tile's columns
+        const int pw = warp - 4;            // 0 .. PROMO_WARPS-1
+        const int half = pw >> 2;           // which column group of the tile
         const int quarter = warp & 3;       // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
         uint8_t* my_out = sOut + pw * (CPW / 64) * Cfg::BOX_BYTES;
@@ -378,30 +403,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t sc2 = pack_f32x2(sc, sc);
             const uint32_t t_base =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BN + half * CPW;
+            constexpr int LW = Cfg::LW;
 #pragma unroll
-            for (int j = 0; j < CPW / 64; ++j) {
-                uint64_t p[32];  // columns j*64 .. j*64+63 of the partial sums, as pairs
-                tmem_ld_x64_pairs(t_base + j * 64, p);
-                if (j == CPW / 64 - 1) {
+            for (int j = 0; j < CPW / LW; ++j) {
+                uint64_t p[LW / 2];  // columns j*LW .. j*LW+LW-1 of the partial sums, as pairs
+                tmem_ld_pairs<LW>(t_base + j * LW, p);
+                if (j == CPW / LW - 1) {
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&tempty[b]);
                 }
-                uint64_t* a = acc + j * 32;
+                uint64_t* a = acc + j * (LW / 2);
                 if (Cfg::SB_VEC) {
                     // per-column scales: broadcast 16-byte shared-memory reads (two column pairs each)
                     const ulonglong2* sbv =
-                        reinterpret_cast<const ulonglong2*>(sSB + ss * Cfg::BN + half * CPW + j * 64);
+                        reinterpret_cast<const ulonglong2*>(sSB + ss * Cfg::BN + half * CPW + j * LW);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < LW / 4; ++i) {
                         const ulonglong2 v = sbv[i];
                         ffma2(a[2 * i], fmul2(p[2 * i], v.x), sa2);
                         ffma2(a[2 * i + 1], fmul2(p[2 * i + 1], v.y), sa2);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
+                    for (int i = 0; i < LW / 2; ++i)
                         ffma2(a[i], p[i], sc2);
                 }
             }

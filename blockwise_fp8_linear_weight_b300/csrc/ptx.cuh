@@ -348,6 +348,35 @@ __device__ __forceinline__ void tmem_ld_x64_pairs(uint32_t taddr, uint64_t (&p)[
         : "memory");
 }
 
+// As tmem_ld_x64_pairs for 32 columns (16 pairs).
+__device__ __forceinline__ void tmem_ld_x32_pairs(uint32_t taddr, uint64_t (&p)[16])
+{
+    asm volatile(
+        "{\n\t.reg .b32 r<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, "
+        "r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
+        "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t"
+        "mov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
+        "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\t}"
+        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]),
+          "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <int NCOLS>
+__device__ __forceinline__ void tmem_ld_pairs(uint32_t taddr, uint64_t (&p)[NCOLS / 2])
+{
+    static_assert(NCOLS == 32 || NCOLS == 64, "32 or 64 columns");
+    if constexpr (NCOLS == 64)
+        tmem_ld_x64_pairs(taddr, p);
+    else
+        tmem_ld_x32_pairs(taddr, p);
+}
+
 // d = a * s on packed pairs
 __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t s)
 {

@@ -274,19 +274,37 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + (i & 1) * kQuantTileBytes);
 
         if (MODE == MODE_ROWS || MODE == MODE_DUAL) {
-            // thread t: rows t/16 + 16 j, columns 8 (t%16) .. +7; a half-warp owns one row tile
-#pragma unroll 2
+            // thread t: rows t/16 + 16 j, columns 8 (t%16) .. +7; a half-warp owns one
+            // row tile per j, so a warp owns 16 tiles. Their amax values are gathered
+            // so that lane (16 h + j) holds tile (j, half-warp h), each lane computes one
+            // tile scale, and the encoding pass fetches its tile's scale by shuffle:
+            // one scale computation per warp instead of one per 8 elements.
+            float my_amax = 0.0f;
+#pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int row = (tid >> 4) + 16 * j;
-                const int64_t gr = rb * 128 + row;
-                const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
-                uint32_t m = absmax_pairs(v);
+                uint32_t m = absmax_pairs(*reinterpret_cast<const uint4*>(&tile[row][sub * 4]));
                 m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 8));
                 m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 4));
                 m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 2));
                 m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                if (sub == j)
+                    my_amax = fmaxf(bf16_lo(m), bf16_hi(m));
+            }
+            const TileScale mine = tile_scale(my_amax);
+            const int lane = tid & 31;
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                const int src = (lane & 16) | j;
+                TileScale ts;
+                ts.s = __shfl_sync(0xffffffffu, mine.s, src);
+                ts.pre = __shfl_sync(0xffffffffu, mine.pre, src);
+                ts.sp = __shfl_sync(0xffffffffu, mine.sp, src);
+                ts.y = __shfl_sync(0xffffffffu, mine.y, src);
+                const int row = (tid >> 4) + 16 * j;
+                const int64_t gr = rb * 128 + row;
                 if (gr < a.R) {
-                    const TileScale ts = tile_scale(fmaxf(bf16_lo(m), bf16_hi(m)));
+                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
                     *reinterpret_cast<uint2*>(a.q + gr * a.ldq + cb * 128 + sub * 8) =
                         codes8_packed(v, pair_scale(ts, ts));
                     if (sub == 0)

@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
                           "fp8_quantize_act_transpose",
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
-                          "bfp8_set_gemm_cluster"}
+                          "bfp8_set_gemm_cluster", "bfp8_set_gemm_promo_warps"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
         assert hasattr(cdll, n), n
@@ -40,6 +40,9 @@ def test_tile_knob(lib):
     assert lib.bfp8_set_gemm_tile_n(64) == EINVAL
     prev = lib.bfp8_set_gemm_tile_n(256)
     assert lib.bfp8_set_gemm_tile_n(prev) == 256
+    assert lib.bfp8_set_gemm_promo_warps(12) == EINVAL
+    prev = lib.bfp8_set_gemm_promo_warps(16)
+    assert lib.bfp8_set_gemm_promo_warps(prev) == 16
     assert lib.bfp8_set_gemm_cluster(3) == EINVAL
     prev = lib.bfp8_set_gemm_cluster(1)
     assert lib.bfp8_set_gemm_cluster(prev) == 1
