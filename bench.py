@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the side measurements (cuBLAS BF16 comparator, FP32-accumulating wgrad, "
+                        "weight-quantisation reuse)")
     p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 256], help="GEMM tile width (0: automatic)")
     p.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2], help="GEMM CTAs per cluster (0: automatic)")
     p.add_argument("--gemm-promo-warps", type=int, default=0, choices=[0, 8, 16],
@@ -365,6 +368,11 @@ def run_ours(args):
                                 f"FP8/BF16 nominal dense ratio 2" if gemm_dom else
                                 f"{peak_src}: hbm_gbs ({hbm_peak})")}
 
+    extras = None
+    if not args.no_extras and not fwd_only:
+        extras = side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, tflops,
+                                   min(args.steps, 200), dev)
+
     # ------------------------------------------------------------ end to end (host buffers)
     # Every step copies x, W and dy of every linear in from pinned host memory and
     # y, dx and dW out, through the public API. Copies in, compute and copies out
@@ -452,7 +460,7 @@ def run_ours(args):
                                                           for l in work.linears],
                        "passes": "+".join(work.passes) + " incl. all quantisers",
                        "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (no flush)"},
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "extras": extras,
             "gpu_launches": kernels_per_step * args.steps, "clocks": clocks,
             "device_status": bfp8.STATUS.get(status, status),
         }
@@ -460,6 +468,79 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_tflops, steps, dev):
+    """Measurements next to the headline number, outside its timed region (CUDA events,
+    3 warm-up steps each, same inputs):
+      bf16_cublas: the same three GEMMs per linear in BF16 through torch.matmul (cuBLAS), the
+        comparator for the FP8 path's speed-up (the Puro-2B write-up quotes 1.36x FP8 over
+        BF16 on its RTX 5090s);
+      wgrad_fp32_acc: the weight-gradient GEMM accumulating into an FP32 main gradient;
+      weight_quant_reuse: the training step of a micro-batch after the first, W's codes reused
+        (five kernels per linear)."""
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    out = {}
+    # cuBLAS BF16: y = x W^T, dx = dy W, dW = dy^T x into preallocated outputs
+    bufs = [(torch.empty((l.M, l.N), dtype=torch.bfloat16, device=dev),
+             torch.empty((l.M, l.K), dtype=torch.bfloat16, device=dev),
+             torch.empty((l.N, l.K), dtype=torch.bfloat16, device=dev)) for l in work.linears]
+
+    def bf16_step():
+        for (x, w, dy), (y, dx, dw) in zip(inputs, bufs):
+            torch.matmul(x, w.t(), out=y)
+            torch.matmul(dy, w, out=dx)
+            torch.matmul(dy.t(), x, out=dw)
+
+    ms_bf16 = timed(bf16_step, steps)
+    bf16_tflops = work.flops / (ms_bf16 / 1e3) / 1e12
+    out["bf16_cublas"] = {"tflops": round(bf16_tflops, 1), "ms_per_step": round(ms_bf16, 4),
+                          "fp8_speedup": round(fp8_tflops / bf16_tflops, 3),
+                          "what": "torch.matmul BF16 (cuBLAS) for fwd, dgrad and wgrad of every linear, "
+                                  "no quantisers; fp8_speedup = FP8 step (quantisers included) over this"}
+
+    # wgrad into an FP32 main gradient, one launch per linear
+    mgs = [torch.zeros((l.N, l.K), dtype=torch.float32, device=dev) for l in work.linears]
+
+    def acc_step():
+        for L, l, mg in zip(layers, work.linears, mgs):
+            bfp8.fp8_block_gemm_wgrad_acc(L.qdyt, L.sdyt, L.qxt, L.sxt, l.M, mg)
+
+    ms_acc = timed(acc_step, steps)
+    acc_tflops = sum(2 * l.M * l.N * l.K for l in work.linears) / (ms_acc / 1e3) / 1e12
+    out["wgrad_fp32_acc"] = {"tflops": round(acc_tflops, 1), "frac_of_peak": round(acc_tflops / fp8_peak, 4),
+                             "avg_us_per_launch": round(1e3 * ms_acc / len(layers), 2)}
+
+    # micro-batches after the first: W unchanged, its codes reused
+    for L in layers:
+        L.reuse_weight_quant = True
+        L.invalidate_weight_quant()
+
+    def reuse_step():
+        for L, (x, w, dy) in zip(layers, inputs):
+            L.forward(x, w)
+            L.backward(dy)
+
+    ms_reuse = timed(reuse_step, steps)
+    for L in layers:
+        L.reuse_weight_quant = False
+    out["weight_quant_reuse"] = {"tflops": round(work.flops / (ms_reuse / 1e3) / 1e12, 1),
+                                 "ms_per_step": round(ms_reuse, 4),
+                                 "kernels_per_step": 5 * len(layers)}
+    out["steps_each"] = steps
+    return out
 
 
 def dual_bytes(R: int, C: int) -> int:

@@ -14,6 +14,7 @@ Entry points (same names as the C ABI):
   fp8_block_gemm_fwd(qx, sx, qw, sw)        -> y  [M, N] bf16
   fp8_block_gemm_dgrad(qdy, sdy, qw, sw)    -> dx [M, K] bf16
   fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M) -> dw [N, K] bf16
+  fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad): main_grad [N, K] f32 += dW
 Scale tensors are allocated with a row stride rounded up to 4 elements so that
 the GEMMs' TMA loads see 16-byte rows; the returned tensors are views of the
 valid columns.
@@ -63,6 +64,7 @@ def load_library(path: str = LIB_PATH):
         "fp8_block_gemm_fwd": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
         "fp8_block_gemm_dgrad": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
         "fp8_block_gemm_wgrad": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
+        "fp8_block_gemm_wgrad_acc": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
         "bfp8_last_device_status": [p],
         "bfp8_set_gemm_tile_n": [c_int],
         "bfp8_set_gemm_cluster": [c_int],
@@ -215,6 +217,18 @@ def fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M, dw=None):
     return dw
 
 
+def fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad):
+    """main_grad [N, K] f32 += blockwise-FP8 dy^T x (FP32 sum, no BF16 rounding), in place."""
+    lib = load_library()
+    N = qdyt.shape[0]
+    K = qxt.shape[0]
+    _req(main_grad, torch.float32, "main_grad")
+    _check("fp8_block_gemm_wgrad_acc", lib.fp8_block_gemm_wgrad_acc(
+        _ptr(qdyt), qdyt.stride(0), _ptr(sdyt), sdyt.stride(0), _ptr(qxt), qxt.stride(0),
+        _ptr(sxt), sxt.stride(0), _ptr(main_grad), main_grad.stride(0), M, N, K, _stream()))
+    return main_grad
+
+
 def last_device_status() -> int:
     """Synchronise the current stream and read/clear the kernels' bounded-wait status word."""
     return load_library().bfp8_last_device_status(_stream())
@@ -254,12 +268,27 @@ class BlockwiseFP8Linear:
     both layouts and runs the input- and weight-gradient GEMMs. All outputs
     live in buffers allocated once, so a training step launches exactly six
     kernels and allocates nothing.
+
+    Options:
+      reuse_weight_quant: keep W's codes and scales while W is unchanged (same
+        storage, same torch version counter), so that micro-batches after the
+        first of an optimizer step skip the weight quantiser (five kernels).
+        The FP8 copy is derived, non-persistent state: it is rebuilt from W
+        whenever W changes and never needs saving.
+      main_grad: accumulate dW into an FP32 main-gradient buffer
+        (``self.main_grad``, zeroed by ``zero_main_grad()``) instead of writing
+        a BF16 dW, as a trainer keeping its state in FP32 does across
+        micro-batches.
     """
 
     KERNELS_PER_STEP = 6
 
-    def __init__(self, M: int, K: int, N: int, device="cuda"):
+    def __init__(self, M: int, K: int, N: int, device="cuda", reuse_weight_quant: bool = False,
+                 main_grad: bool = False):
         self.M, self.K, self.N = M, K, N
+        self.reuse_weight_quant = reuse_weight_quant
+        self.weight_quant_calls = 0
+        self._w_key = None
         dev = torch.device(device)
         M128 = _round_up(M, TILE)
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
@@ -275,16 +304,37 @@ class BlockwiseFP8Linear:
         self.sxt = _scales(M128 // TILE, K, dev)
         self.y = torch.empty((M, N), dtype=bf, device=dev)
         self.dx = torch.empty((M, K), dtype=bf, device=dev)
-        self.dw = torch.empty((N, K), dtype=bf, device=dev)
+        self.dw = None if main_grad else torch.empty((N, K), dtype=bf, device=dev)
+        self.main_grad = torch.zeros((N, K), dtype=f32, device=dev) if main_grad else None
+
+    def quantize_weight(self, w):
+        """Quantise W unless reuse is on and W is the tensor (and version) quantised last."""
+        key = (w.data_ptr(), w._version, tuple(w.shape), tuple(w.stride()))
+        if self.reuse_weight_quant and key == self._w_key:
+            return
+        fp8_quantize_weight(w, self.qw, self.sw)
+        self.weight_quant_calls += 1
+        self._w_key = key
+
+    def invalidate_weight_quant(self):
+        """Forget the cached weight codes (e.g. after W was changed behind torch's back)."""
+        self._w_key = None
+
+    def zero_main_grad(self):
+        self.main_grad.zero_()
 
     def forward(self, x, w):
         fp8_quantize_act_transpose(x, self.qx, self.sx, self.qxt, self.sxt)
-        fp8_quantize_weight(w, self.qw, self.sw)
+        self.quantize_weight(w)
         fp8_block_gemm_fwd(self.qx, self.sx, self.qw, self.sw, self.y)
         return self.y
 
     def backward(self, dy):
+        """Returns (dx, dW): dW is the BF16 buffer, or the FP32 main gradient it was added into."""
         fp8_quantize_act_transpose(dy, self.qdy, self.sdy, self.qdyt, self.sdyt)
         fp8_block_gemm_dgrad(self.qdy, self.sdy, self.qw, self.sw, self.dx)
+        if self.main_grad is not None:
+            fp8_block_gemm_wgrad_acc(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.main_grad)
+            return self.dx, self.main_grad
         fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw)
         return self.dx, self.dw

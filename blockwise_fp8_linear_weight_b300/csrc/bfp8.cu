@@ -192,8 +192,12 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
                             CU_TENSOR_MAP_SWIZZLE_NONE);
     else
         tmSB = tmSA;  // unused in scalar mode
-    ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.d, p.gn, p.gm, p.ldd * 2, 64, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (Cfg::EPI == EPI_F32_ADD)
+        ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.d, p.gn, p.gm, p.ldd * 4, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.d, p.gn, p.gm, p.ldd * 2, 64, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok)
         return BFP8_ELAUNCH;
 
@@ -248,7 +252,7 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     return launch_status();
 }
 
-template <bool B_MN, bool SB_VEC>
+template <bool B_MN, bool SB_VEC, int EPI = EPI_BF16_TMA>
 int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
 {
     int dev = 0;
@@ -258,6 +262,8 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
     unsigned* status = device_status_ptr(dev);
     if (!status)
         return BFP8_ELAUNCH;
+    if (EPI == EPI_F32_ADD)  // one configuration: 256-wide tiles, one CTA per cluster, 8 promotion warps
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1, EPI_F32_ADD>>(p, status, stream, dev);
     int tn = g_tile_n.load(std::memory_order_relaxed);
     if (tn == 0)
         tn = 256;
@@ -530,6 +536,41 @@ extern "C" int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const f
     p.gn = K;
     p.gk = M128;
     return dispatch_gemm<false, true>(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
+                                        const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
+                                        float* main_grad, int64_t ldmg, int64_t M, int64_t N, int64_t K,
+                                        void* stream)
+{
+    if (M < 0 || N < 0 || K < 0)
+        return BFP8_EINVAL;
+    const int64_t M128 = (M + 127) / 128 * 128;
+    if (M < 1 || !gemm_dims_ok(N, K, M128))
+        return BFP8_ESHAPE;
+    if (!qdyt || !sdyt || !qxt || !sxt || !main_grad || ldqdyt < M128 || ldqxt < M128 || ldsdyt < N ||
+        ldsxt < K || ldmg < K)
+        return BFP8_EINVAL;
+    if (!aligned(qdyt, 16) || !aligned(qxt, 16) || !aligned(sdyt, 16) || !aligned(sxt, 16) ||
+        !aligned(main_grad, 16) || ldqdyt % 16 || ldqxt % 16 || ldsdyt % 4 || ldsxt % 4 || ldmg % 4)
+        return BFP8_EALIGN;
+    GemmProblem p{};
+    p.a = qdyt;
+    p.lda = ldqdyt;
+    p.b = qxt;
+    p.ldb = ldqxt;
+    p.b_mn = false;
+    p.sa = sdyt;
+    p.ld_sa = ldsdyt;
+    p.sb = sxt;
+    p.ld_sb = ldsxt;
+    p.sb_vec = true;
+    p.d = main_grad;
+    p.ldd = ldmg;
+    p.gm = N;
+    p.gn = K;
+    p.gk = M128;
+    return dispatch_gemm<false, true, EPI_F32_ADD>(p, static_cast<cudaStream_t>(stream));
 }
 
 // =================================================================== misc

@@ -35,7 +35,8 @@
 //               tile it rounds acc to BF16, stages it in its own 128-byte-
 //               swizzled shared-memory slab and issues TMA stores (the TMA unit
 //               drops rows and columns outside D), overlapping the MMAs of the
-//               next tile.
+//               next tile. The accumulate epilogue instead stages acc as FP32
+//               and has the TMA unit add it into an FP32 D (D += acc).
 // With BN = 256 the promotion warps need more than the 168 registers a
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
 // warpgroup to the promotion warpgroups (56/224, or 64/216 with per-column
@@ -50,7 +51,14 @@
 
 namespace bfp8 {
 
-template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, bool EPI_SMEM_ = true, int PW_ = 8>
+// Epilogue kinds: what the promotion warps do with a finished tile.
+enum GemmEpilogue {
+    EPI_BF16_DIRECT = 0,  // round to BF16, 16-byte stores straight from registers
+    EPI_BF16_TMA = 1,     // round to BF16, stage in shared memory, TMA store (default)
+    EPI_F32_ADD = 2,      // keep FP32, stage in shared memory, TMA reduce-add into an FP32 D
+};
+
+template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, int EPI_ = EPI_BF16_TMA, int PW_ = 8>
 struct GemmConfig {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -59,11 +67,14 @@ struct GemmConfig {
     static constexpr int SSTAGES = 8;
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
-    // epilogue: true = stage BF16 tiles in shared memory and store them with TMA
-    // (default); false = each thread stores its row's 16-byte groups straight to
-    // global memory, which frees the staging slab for a deeper operand ring but
-    // measured slower (the uncoalesced stores hold up the promotion warps)
-    static constexpr bool EPI_SMEM = EPI_SMEM_;
+    // epilogue: EPI_BF16_TMA stages BF16 tiles in shared memory and stores them
+    // with TMA; EPI_BF16_DIRECT has each thread store its row's 16-byte groups
+    // straight to global memory, which frees the staging slab for a deeper
+    // operand ring but measured slower (the uncoalesced stores hold up the
+    // promotion warps); EPI_F32_ADD stages FP32 boxes in the same slab and adds
+    // them into an FP32 D with TMA reduce-add (D += result, no BF16 rounding)
+    static constexpr int EPI = EPI_;
+    static constexpr bool EPI_SMEM = EPI_ != EPI_BF16_DIRECT;
     // CTAs per cluster along M: the CTAs of a cluster compute vertically adjacent
     // tiles that share one B tile; each loads 1/CLUSTER of it and multicasts it
     static constexpr int CLUSTER = CLUSTER_;
@@ -86,7 +97,8 @@ struct GemmConfig {
     static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;
     static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
     static constexpr uint32_t SC_TX = SA_BYTES + SB_BYTES;
-    // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 64 bf16 (4 KB, 128-byte swizzle)
+    // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
+    // (64 BF16 or 32 FP32 columns; 4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
     static constexpr int STAGE_OUT_BYTES = EPI_SMEM ? PROMO_WARPS * (CPW / 64) * BOX_BYTES : 0;
     // shared-memory layout (offsets from a 1024-byte-aligned base)
@@ -439,7 +451,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (++c == nc) {
                 // ------------------------------------------------ BF16 epilogue of tile t
                 const int col0 = n0 + half * CPW;
-                if constexpr (Cfg::EPI_SMEM) {
+                if constexpr (Cfg::EPI == EPI_F32_ADD) {
+                    // FP32 boxes of 32 columns: the slab holds CPW/64 of them, so the
+                    // CPW/32 boxes of the row go out in two rounds
+                    constexpr int SLAB = CPW / 64;
+#pragma unroll
+                    for (int round = 0; round < 2; ++round) {
+                        if (lane == 0)
+                            tma_store_wait_read_all();  // earlier adds have read the slab
+                        __syncwarp();
+#pragma unroll
+                        for (int bx = 0; bx < SLAB; ++bx) {
+                            uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
+                            const uint64_t* v = acc + (round * SLAB + bx) * 16;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const uint4 pk = make_uint4(static_cast<uint32_t>(v[2 * k]),
+                                                            static_cast<uint32_t>(v[2 * k] >> 32),
+                                                            static_cast<uint32_t>(v[2 * k + 1]),
+                                                            static_cast<uint32_t>(v[2 * k + 1] >> 32));
+                                *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int bx = 0; bx < SLAB; ++bx) {
+                                const int x = col0 + (round * SLAB + bx) * 32;
+                                if (x < args.gn && m0 + quarter * 32 < args.gm)
+                                    tma_reduce_add_2d(&tmD, my_out + bx * Cfg::BOX_BYTES, x, m0 + quarter * 32);
+                            }
+                            tma_store_commit();
+                        }
+                    }
+                } else if constexpr (Cfg::EPI == EPI_BF16_TMA) {
                     if (lane == 0)
                         tma_store_wait_read_all();  // this warp's previous stores have left the slab
                     __syncwarp();

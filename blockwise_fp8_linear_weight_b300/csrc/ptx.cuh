@@ -176,6 +176,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                  : "memory");
 }
 
+// Element-wise reduce-add of a shared-memory box into global memory through a
+// tensor map (FP32 here): every element of the box is added to its global
+// counterpart by the TMA unit; boxes past the tensor's edge are dropped.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y)
+{
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

@@ -22,11 +22,14 @@
 // identical to the IEEE division. To keep the remainders clear of the
 // subnormal range, tiles with a scale below 2^-60 (including binary32
 // subnormal scales) work on a and s both multiplied by 2^64, which changes
-// neither the quotient nor any rounding. The quotient is taken of |x| and given
-// x's sign afterwards, so that -0 keeps its sign; an all-zero tile (s = 0)
-// runs the same instructions with y = 0 and yields the inputs' signed zeros.
-// Where a is so small against s that a remainder still underflows, the
-// quotient is below 2^-40 and its code is a signed zero either way.
+// neither the quotient nor any rounding. The steps are odd in a (every
+// rounding is to nearest-even), so the quotient of a signed x carries x's
+// sign, except that an exact zero comes out as +0: x's sign bit is therefore
+// OR-ed into the code afterwards, which keeps -0 (and negative quotients that
+// round to zero) as 0x80. An all-zero tile (s = 0) runs the same instructions
+// with y = 0 and yields the inputs' signed zeros. Where a is so small against
+// s that a remainder still underflows, the quotient is below 2^-40 and its
+// code is a signed zero either way.
 //
 // All four kernels are HBM-bound (2 B read + 1 B written per element and per
 // code layout): reads are 16-byte vector loads that cover whole 128-byte lines,
@@ -35,6 +38,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -61,8 +65,8 @@ __device__ __forceinline__ TileScale tile_scale(float amax)
 // ---------------------------------------------------------------------------
 // Packed form used by the kernels: two values per 64-bit register pair, so the
 // five quotient steps (one product, two Markstein corrections) are five packed
-// FP32 instructions per pair. Inputs are the magnitudes |x| (the sign is put
-// back into the code bytes), and lane i of every operand belongs to value i.
+// FP32 instructions per pair (six for tiles that need the 2^64 pre-scaling,
+// which take a separate code path). Lane i of every operand belongs to value i.
 // ---------------------------------------------------------------------------
 struct PairScale {
     uint64_t ns;   // {-sp_lo, -sp_hi}
@@ -81,17 +85,18 @@ __device__ __forceinline__ PairScale pair_scale(const TileScale& lo, const TileS
     return p;
 }
 
-// |values| of a packed BF16 pair as a packed FP32 pair
-__device__ __forceinline__ uint64_t unpack_abs(uint32_t w)
+// a packed BF16 pair as a packed FP32 pair (exact)
+__device__ __forceinline__ uint64_t unpack2(uint32_t w)
 {
-    const uint32_t aw = w & 0x7FFF7FFFu;
-    return pack_f32x2(__uint_as_float(aw << 16), __uint_as_float(aw & 0xFFFF0000u));
+    return pack_f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// RN(a / s) lane-wise for a packed pair of magnitudes
+// RN(a / s) lane-wise for a packed pair (SCALED: the tile pair has a 2^64
+// pre-scaling factor; the kernels branch on PairScale::scaled)
+template <bool SCALED>
 __device__ __forceinline__ uint64_t quotient2(uint64_t a, const PairScale& ps)
 {
-    if (ps.scaled)
+    if (SCALED)
         a = fmul2(a, ps.pre);
     uint64_t q = fmul2(a, ps.y);
     uint64_t r = a;
@@ -103,7 +108,7 @@ __device__ __forceinline__ uint64_t quotient2(uint64_t a, const PairScale& ps)
     return q;
 }
 
-// E4M3 codes of a packed FP32 pair (non-negative): low value in bits 0-7
+// E4M3 codes of a packed FP32 pair: low value in bits 0-7, high in bits 8-15
 __device__ __forceinline__ uint32_t cvt_e4m3x2(uint64_t q)
 {
     uint16_t r;
@@ -115,6 +120,27 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(uint64_t q)
     return r;
 }
 
+// E4M3 codes of two packed FP32 pairs as one word: bytes q01.lo, q01.hi, q23.lo, q23.hi
+__device__ __forceinline__ uint32_t cvt_e4m3x4(uint64_t q01, uint64_t q23)
+{
+    uint32_t r;
+    asm("{\n\t.reg .f32 a0, a1, b0, b1;\n\t.reg .b16 c0, c1;\n\t"
+        "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 c0, a1, a0;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 c1, b1, b0;\n\t"
+        "mov.b32 %0, {c0, c1};\n\t}"
+        : "=r"(r)
+        : "l"(q01), "l"(q23));
+    return r;
+}
+
+// Sign bits of two BF16 pair words, placed as the sign bits of the four codes
+// that cvt_e4m3x4 makes of them (bit 7 of bytes 1 and 3 of each word)
+__device__ __forceinline__ uint32_t sign_bits4(uint32_t w01, uint32_t w23)
+{
+    return __byte_perm(w01, w23, 0x7531) & 0x80808080u;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
     uint32_t d;
@@ -122,24 +148,33 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
     return d;
 }
 
+// lane-wise max(|a|, |b|) of two BF16 pairs, each lane's sign bit the XOR of
+// the inputs' (callers clear the sign bits once, after the last step)
+__device__ __forceinline__ uint32_t bf16x2_maxabs(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // lane-wise max of |values| over the 4 BF16 pairs of a 16-byte vector
 __device__ __forceinline__ uint32_t absmax_pairs(const uint4& v)
 {
-    return bf16x2_max(bf16x2_max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                      bf16x2_max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return bf16x2_maxabs(bf16x2_maxabs(v.x, v.y), bf16x2_maxabs(v.z, v.w)) & 0x7FFF7FFFu;
 }
 
 // 8 BF16 values sharing one tile scale -> 8 codes (first value in the low byte)
+template <bool SCALED>
 __device__ __forceinline__ uint2 codes8_packed(const uint4& v, const PairScale& ps)
 {
-    const uint32_t c0 = cvt_e4m3x2(quotient2(unpack_abs(v.x), ps));
-    const uint32_t c1 = cvt_e4m3x2(quotient2(unpack_abs(v.y), ps));
-    const uint32_t c2 = cvt_e4m3x2(quotient2(unpack_abs(v.z), ps));
-    const uint32_t c3 = cvt_e4m3x2(quotient2(unpack_abs(v.w), ps));
-    // sign bits: bit 7 of bytes 1 and 3 of each BF16 pair word
-    const uint32_t s01 = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
-    const uint32_t s23 = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
-    return make_uint2((c0 | (c1 << 16)) | s01, (c2 | (c3 << 16)) | s23);
+    const uint32_t lo = cvt_e4m3x4(quotient2<SCALED>(unpack2(v.x), ps), quotient2<SCALED>(unpack2(v.y), ps));
+    const uint32_t hi = cvt_e4m3x4(quotient2<SCALED>(unpack2(v.z), ps), quotient2<SCALED>(unpack2(v.w), ps));
+    return make_uint2(lo | sign_bits4(v.x, v.y), hi | sign_bits4(v.z, v.w));
+}
+
+__device__ __forceinline__ uint2 codes8(const uint4& v, const PairScale& ps)
+{
+    return ps.scaled ? codes8_packed<true>(v, ps) : codes8_packed<false>(v, ps);
 }
 
 // ---------------------------------------------------------------------------
@@ -151,6 +186,26 @@ __device__ __forceinline__ uint2 codes8_packed(const uint4& v, const PairScale& 
 // amax through shared memory. Codes go to qt [C][R128] (row = input column),
 // scales to st [R128/128][C]. Pad rows hold +0 and so get code 0x00.
 // ---------------------------------------------------------------------------
+template <bool SCALED>
+__device__ __forceinline__ void column_encode(const uint32_t (*tile)[64], int quarter, int cw, const PairScale& ps,
+                                              uint32_t (&c0)[8], uint32_t (&c1)[8])
+{
+    // rows in groups of 4: the row pair words w0..w3 give the codes of (row, col)
+    // and (row, col + 1); cvt_e4m3x4 packs rows 0-1 and rows 2-3, byte_perm
+    // regroups them by column
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = quarter * 32 + 4 * j;
+        const uint32_t w0 = tile[r][cw], w1 = tile[r + 1][cw], w2 = tile[r + 2][cw], w3 = tile[r + 3][cw];
+        const uint32_t a = cvt_e4m3x4(quotient2<SCALED>(unpack2(w0), ps), quotient2<SCALED>(unpack2(w1), ps)) |
+                           sign_bits4(w0, w1);
+        const uint32_t b = cvt_e4m3x4(quotient2<SCALED>(unpack2(w2), ps), quotient2<SCALED>(unpack2(w3), ps)) |
+                           sign_bits4(w2, w3);
+        c0[j] = __byte_perm(a, b, 0x6420);
+        c1[j] = __byte_perm(a, b, 0x7531);
+    }
+}
+
 __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t (*part)[64], int64_t cb, int64_t rb,
                                             uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ st,
                                             int64_t ldst)
@@ -164,27 +219,18 @@ __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-        m = bf16x2_max(m, tile[quarter * 32 + i][cw] & 0x7FFF7FFFu);
-    part[quarter][cw] = m;
+        m = bf16x2_maxabs(m, tile[quarter * 32 + i][cw]);
+    part[quarter][cw] = m & 0x7FFF7FFFu;
     __syncthreads();
     m = bf16x2_max(bf16x2_max(part[0][cw], part[1][cw]), bf16x2_max(part[2][cw], part[3][cw]));
     const TileScale s0 = tile_scale(bf16_lo(m)), s1 = tile_scale(bf16_hi(m));
     const PairScale ps = pair_scale(s0, s1);
 
-    // rows in groups of 4: each row's pair gives code(col) in byte 0, code(col+1) in byte 1
     uint32_t c0[8], c1[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t c[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = tile[quarter * 32 + 4 * j + i][cw];
-            c[i] = cvt_e4m3x2(quotient2(unpack_abs(w), ps)) | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
-        }
-        const uint32_t a = c[0] | (c[1] << 16), b = c[2] | (c[3] << 16);
-        c0[j] = __byte_perm(a, b, 0x6420);
-        c1[j] = __byte_perm(a, b, 0x7531);
-    }
+    if (ps.scaled)
+        column_encode<true>(tile, quarter, cw, ps, c0, c1);
+    else
+        column_encode<false>(tile, quarter, cw, ps, c0, c1);
     uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + quarter * 32;
     uint8_t* out1 = out0 + ldqt;
     reinterpret_cast<uint4*>(out0)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
@@ -275,27 +321,37 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
 
         if (MODE == MODE_ROWS || MODE == MODE_DUAL) {
             // thread t: rows t/16 + 16 j, columns 8 (t%16) .. +7; a half-warp owns one
-            // row tile per j, so a warp owns 16 tiles. Their amax values are gathered
-            // so that lane (16 h + j) holds tile (j, half-warp h), each lane computes one
-            // tile scale, and the encoding pass fetches its tile's scale by shuffle:
-            // one scale computation per warp instead of one per 8 elements.
-            float my_amax = 0.0f;
+            // row tile per j (j = 0..7). The half-warp reduces its 8 tiles at once
+            // with a butterfly that halves the number of tiles each lane carries
+            // per step (lane bit 3 picks 4 of the 8, bit 2 two of those, bit 1
+            // one), so that lanes 2j and 2j+1 end with tile j's amax; each lane
+            // computes that tile's scale, and the encoding pass fetches a tile's
+            // scale by shuffle.
+            uint32_t m[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int row = (tid >> 4) + 16 * j;
-                uint32_t m = absmax_pairs(*reinterpret_cast<const uint4*>(&tile[row][sub * 4]));
-                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 8));
-                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 4));
-                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                if (sub == j)
-                    my_amax = fmaxf(bf16_lo(m), bf16_hi(m));
+            for (int j = 0; j < 8; ++j)
+                m[j] = absmax_pairs(*reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4]));
+            {
+                const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t send = b3 ? m[i] : m[i + 4], keep = b3 ? m[i + 4] : m[i];
+                    m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t send = b2 ? m[i] : m[i + 2], keep = b2 ? m[i + 2] : m[i];
+                    m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+                }
+                const uint32_t send = b1 ? m[0] : m[1], keep = b1 ? m[1] : m[0];
+                m[0] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+                m[0] = bf16x2_max(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
             }
-            const TileScale mine = tile_scale(my_amax);
+            const TileScale mine = tile_scale(fmaxf(bf16_lo(m[0]), bf16_hi(m[0])));  // tile (sub >> 1)
             const int lane = tid & 31;
 #pragma unroll 2
             for (int j = 0; j < 8; ++j) {
-                const int src = (lane & 16) | j;
+                const int src = (lane & 16) | (2 * j);
                 TileScale ts;
                 ts.s = __shfl_sync(0xffffffffu, mine.s, src);
                 ts.pre = __shfl_sync(0xffffffffu, mine.pre, src);
@@ -305,8 +361,7 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
                 const int64_t gr = rb * 128 + row;
                 if (gr < a.R) {
                     const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
-                    *reinterpret_cast<uint2*>(a.q + gr * a.ldq + cb * 128 + sub * 8) =
-                        codes8_packed(v, pair_scale(ts, ts));
+                    *reinterpret_cast<uint2*>(a.q + gr * a.ldq + cb * 128 + sub * 8) = codes8(v, pair_scale(ts, ts));
                     if (sub == 0)
                         a.s[cb * a.lds + gr] = ts.s;
                 }
@@ -331,12 +386,19 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
                 m = bf16x2_max(m, red[k]);
             const TileScale ts = tile_scale(fmaxf(bf16_lo(m), bf16_hi(m)));
             const PairScale ps = pair_scale(ts, ts);
+            auto encode = [&](auto scaled) {
 #pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                const int row = (tid >> 4) + 16 * j;
-                const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
-                *reinterpret_cast<uint2*>(a.q + (rb * 128 + row) * a.ldq + cb * 128 + sub * 8) = codes8_packed(v, ps);
-            }
+                for (int j = 0; j < 8; ++j) {
+                    const int row = (tid >> 4) + 16 * j;
+                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
+                    *reinterpret_cast<uint2*>(a.q + (rb * 128 + row) * a.ldq + cb * 128 + sub * 8) =
+                        codes8_packed<decltype(scaled)::value>(v, ps);
+                }
+            };
+            if (ps.scaled)
+                encode(std::true_type{});
+            else
+                encode(std::false_type{});
             if (tid == 0)
                 a.s[rb * a.lds + cb] = ts.s;
         }

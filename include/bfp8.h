@@ -125,6 +125,20 @@ int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt,
                          const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
                          void* dw, int64_t lddw, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* Weight-gradient GEMM accumulated into an FP32 main gradient (the recipe
+ * keeps training state in FP32; same article and section as above):
+ *   main_grad[n][k] += sum_mb sdyt[mb][n] * sxt[mb][k] * sum_{m in mb} qdyt[n][m] qxt[k][m]
+ * The sum is formed exactly as in fp8_block_gemm_wgrad, in FP32, and is not
+ * rounded to BF16: the TMA unit adds each FP32 element into main_grad (one
+ * FP32 add per element and call, round to nearest-even; subnormal sums may be
+ * flushed to zero). Operands as fp8_block_gemm_wgrad; main_grad [N][K] FP32
+ * (ldmg) is read and written in place. Each element is updated atomically, so
+ * calls that target the same buffer add up in either order.
+ * Alignment: as fp8_block_gemm_wgrad, with main_grad 16 B and ldmg % 4 == 0. */
+int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
+                             const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
+                             float* main_grad, int64_t ldmg, int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Human-readable name of a bfp8_status value (static string, never NULL). */
 const char* bfp8_status_string(int status);
 

@@ -221,3 +221,15 @@ def gemm_wgrad(qdyt, sdyt, qxt, sxt, M, rows=None):
     lib.oracle_gemm_wgrad(_ptr(qdyt), M128, _ptr(sdyt), N, _ptr(qxt), M128, _ptr(sxt), K,
                           M, N, K, _ptr(r) if r is not None else None, nr, _ptr(dw))
     return dw
+
+
+def gemm_wgrad_accumulate(main_grad, qdyt, sdyt, qxt, sxt, M, rows=None):
+    """main_grad + dW in FP64: the weight gradient added into an FP32 main gradient
+    (the Puro-2B article keeps training state in FP32; section "FP8 takes advantage
+    of the RTX 5090's low precision efficiency"). main_grad [N,K] float32 is not
+    modified; returns [rows, K] float64 = main_grad[rows] + gemm_wgrad(...)."""
+    main = np.asarray(main_grad, dtype=np.float32)
+    dw = gemm_wgrad(qdyt, sdyt, qxt, sxt, M, rows=rows)
+    base = main if rows is None else main[_c(rows, np.int64)]
+    assert base.shape == dw.shape
+    return base.astype(np.float64) + dw

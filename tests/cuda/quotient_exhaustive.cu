@@ -5,8 +5,9 @@
 // another admissible value in the high lane, checked as well), exactly as the
 // kernels compute it. Two counts, both must be zero:
 //   code mismatches: E4M3 code of the quotient differs from that of x / s;
-//   quotient mismatches: the quotient's bits differ from x / s, counted where
-//     |x / s| >= 2^-12 (below 2^-10 every code is a signed zero).
+//   quotient mismatches: the quotient's bits (sign included) differ from
+//     x / s, counted where |x / s| >= 2^-12 (below 2^-10 every code is a
+//     signed zero).
 // For an all-zero tile (amax = 0) the definition's quotient is x itself.
 #include <cstdint>
 #include <cstdio>
@@ -29,18 +30,20 @@ __global__ void check(unsigned long long* pairs, unsigned long long* bad, unsign
         if ((xb2 & 0x7FFFu) > ab)
             xb2 &= 0x8000u;
         const uint32_t w = xb | (xb2 << 16);
-        const uint64_t q = bfp8::quotient2(bfp8::unpack_abs(w), ps);
-        const uint32_t code = bfp8::cvt_e4m3x2(q) | (__byte_perm(w, 0u, 0x4431) & 0x8080u);
+        // the kernels' sequence: signed quotient, codes, then the inputs' sign bits OR-ed in
+        const uint64_t a = bfp8::unpack2(w);
+        const uint64_t q = ps.scaled ? bfp8::quotient2<true>(a, ps) : bfp8::quotient2<false>(a, ps);
+        const uint32_t code = bfp8::cvt_e4m3x4(q, 0) | bfp8::sign_bits4(w, 0u);
         const unsigned vals[2] = {xb, xb2};
 #pragma unroll
         for (int lane = 0; lane < 2; ++lane) {
             const float x = __uint_as_float(vals[lane] << 16);
-            const float ql = __uint_as_float(static_cast<uint32_t>(q >> (32 * lane)));  // |x| / s
+            const float ql = __uint_as_float(static_cast<uint32_t>(q >> (32 * lane)));  // x / s
             const float d = ts.s == 0.0f ? x : __fdiv_rn(x, ts.s);                    // the definition
             ++n;
             const uint32_t want = bfp8::cvt_e4m3x2(d, 0.0f) & 0xFFu;
             const bool code_differs = ((code >> (8 * lane)) & 0xFFu) != want;
-            const bool quot_differs = fabsf(d) >= 0x1p-12f && __float_as_uint(ql) != __float_as_uint(fabsf(d));
+            const bool quot_differs = fabsf(d) >= 0x1p-12f && __float_as_uint(ql) != __float_as_uint(d);
             if (code_differs || quot_differs) {
                 const unsigned long long k = atomicAdd(bad, 1ull);
                 if (k < 4) {

@@ -23,6 +23,7 @@ def test_exports_every_declared_function(lib):
     assert set(names) >= {"fp8_quantize_act", "fp8_quantize_weight", "fp8_quantize_transpose",
                           "fp8_quantize_act_transpose",
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
+                          "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
                           "bfp8_set_gemm_cluster", "bfp8_set_gemm_promo_warps"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
@@ -96,3 +97,11 @@ def test_gemm_argument_checks(lib):
     assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 200, 128, 128, s) == EINVAL
     assert lib.fp8_block_gemm_wgrad(A, 256, A, 126, A, 256, A, 128, A, 128, 200, 128, 128, s) == EINVAL
     assert lib.fp8_block_gemm_wgrad(A, 256, A, 130, A, 256, A, 128, A, 128, 200, 128, 128, s) == EALIGN
+    # wgrad accumulating into FP32: same operand rules, FP32 main gradient with ldmg % 4 == 0
+    acc = lib.fp8_block_gemm_wgrad_acc
+    assert acc(A, 128, A, 128, A, 128, A, 128, A, 128, 0, 128, 128, s) == ESHAPE
+    assert acc(A, 256, A, 128, A, 256, A, 128, A, 128, 200, 128, 96, s) == ESHAPE
+    assert acc(A, 256, A, 128, A, 256, A, 128, None, 128, 200, 128, 128, s) == EINVAL
+    assert acc(A, 256, A, 128, A, 256, A, 128, A, 100, 200, 128, 128, s) == EINVAL  # ldmg < K
+    assert acc(A, 256, A, 128, A, 256, A, 128, A, 130, 200, 128, 128, s) == EALIGN  # ldmg % 4
+    assert acc(A, 256, A, 128, A, 256, A, 128, A + 8, 128, 200, 128, 128, s) == EALIGN

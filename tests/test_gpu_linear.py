@@ -1,0 +1,97 @@
+"""The one-layer call sequence (BlockwiseFP8Linear) on the GPU: its outputs
+against the oracle, the weight-quantisation reuse across micro-batches, and
+the FP32 main-gradient mode.
+
+Bars: codes and scales bit-exact; GEMM outputs within
+|y - y_ref| <= 1e-2 |y_ref| + 1e-3 rms(y_ref) of the oracle's FP64 result from
+the oracle's own codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import from_dev_bf16, gemm_tolerance_ok, to_dev_bf16
+
+import blockwise_fp8_linear_weight_b300 as bfp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(M=300, K=256, N=384):
+    lin = wl.Linear("small", M, K, N, "student_t3", 11)
+    x, w, dy = wl.make_linear(lin)
+    return lin, x, w, dy
+
+
+def _check(got, ref, what):
+    ok, ratio = gemm_tolerance_ok(got, ref)
+    assert ok, f"{what}: worst error/allowance = {ratio:.3g}"
+
+
+def test_layer_step_matches_oracle():
+    lin, x, w, dy = _case()
+    layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N)
+    y = layer.forward(to_dev_bf16(x), to_dev_bf16(w))
+    dx, dw = layer.backward(to_dev_bf16(dy))
+    torch.cuda.synchronize()
+    qx, sx = oracle.quantize_act(x)
+    qw, sw = oracle.quantize_weight(w)
+    qdy, sdy = oracle.quantize_act(dy)
+    qdyt, sdyt = oracle.quantize_transpose(dy)
+    qxt, sxt = oracle.quantize_transpose(x)
+    assert np.array_equal(layer.qw.cpu().numpy(), qw)
+    assert np.array_equal(layer.sw.cpu().numpy().view(np.uint32), sw.view(np.uint32))
+    _check(from_dev_bf16(y), oracle.gemm_fwd(qx, sx, qw, sw), "fwd")
+    _check(from_dev_bf16(dx), oracle.gemm_dgrad(qdy, sdy, qw, sw), "dgrad")
+    _check(from_dev_bf16(dw), oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, lin.M), "wgrad")
+
+
+def test_weight_quantisation_is_reused_until_the_weight_changes():
+    lin, x, w, _ = _case()
+    layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, reuse_weight_quant=True)
+    xd, wd = to_dev_bf16(x), to_dev_bf16(w)
+    y1 = layer.forward(xd, wd).clone()
+    y2 = layer.forward(xd, wd).clone()
+    assert layer.weight_quant_calls == 1
+    assert torch.equal(y1, y2)
+    sw1 = layer.sw.clone()
+    # an in-place update (what an optimizer step does) bumps the version: re-quantised;
+    # a power-of-two factor keeps every code and doubles every scale and output exactly
+    wd.mul_(2.0)
+    y3 = layer.forward(xd, wd).clone()
+    assert layer.weight_quant_calls == 2
+    assert torch.equal(layer.sw, 2.0 * sw1)
+    assert torch.equal(y3, 2.0 * y1)
+    # a different tensor with the same contents is quantised too
+    layer.forward(xd, wd.clone())
+    assert layer.weight_quant_calls == 3
+    # without reuse every forward quantises
+    plain = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N)
+    plain.forward(xd, wd)
+    plain.forward(xd, wd)
+    assert plain.weight_quant_calls == 2
+
+
+def test_main_gradient_mode_accumulates_micro_batches():
+    lin, x, w, dy = _case(M=257, K=384, N=256)
+    xd, wd, dyd = to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy)
+    ref_layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N)
+    ref_layer.forward(xd, wd)
+    _, dw_bf16 = ref_layer.backward(dyd)
+    layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, reuse_weight_quant=True, main_grad=True)
+    assert layer.dw is None
+    layer.forward(xd, wd)
+    _, mg = layer.backward(dyd)
+    torch.cuda.synchronize()
+    # one micro-batch from zero: the FP32 sums round to the BF16 wgrad's output
+    assert torch.equal(mg.to(torch.bfloat16), dw_bf16)
+    once = mg.clone()
+    layer.forward(xd, wd)
+    layer.backward(dyd)
+    torch.cuda.synchronize()
+    assert layer.weight_quant_calls == 1
+    # second micro-batch: once + once, one FP32 rounding per element
+    assert torch.allclose(layer.main_grad, 2.0 * once, rtol=2.0 ** -23, atol=0.0)
+    layer.zero_main_grad()
+    assert torch.count_nonzero(layer.main_grad) == 0

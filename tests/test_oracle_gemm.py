@@ -10,7 +10,9 @@ Checked against facts fixed outside the oracle's own loops:
   * dgrad is fwd with the weight codes and block scales transposed;
   * powers of two on the scales scale the result exactly;
   * end to end, quantise-then-GEMM approximates the BF16 product to within
-    E4M3 precision (this catches a transposed operand or scale anywhere).
+    E4M3 precision (this catches a transposed operand or scale anywhere);
+  * accumulating wgrad into an FP32 main gradient matches brute force plus the
+    main gradient, and accumulating twice from zero doubles dW exactly.
 """
 import ml_dtypes
 import numpy as np
@@ -170,3 +172,37 @@ def test_quantise_then_gemm_approximates_bf16_product(oracle_lib, M):
     qdyt, sdyt = oracle.quantize_transpose(dy)
     qxt, sxt = oracle.quantize_transpose(x)
     assert rel(oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, M), dY.T @ X) < 0.06
+
+
+def _wgrad_operands(M, N, K, seed):
+    M128 = (M + TILE - 1) // TILE * TILE
+    qdyt = random_codes((N, M128), seed)
+    qxt = random_codes((K, M128), seed + 1)
+    qdyt[:, M:] = 0
+    qxt[:, M:] = 0
+    sdyt = random_scales((M128 // TILE, N), seed + 2)
+    sxt = random_scales((M128 // TILE, K), seed + 3)
+    return qdyt, sdyt, qxt, sxt
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (200, 256, 384)])
+def test_wgrad_accumulate_is_main_plus_brute_force(oracle_lib, M, N, K):
+    qdyt, sdyt, qxt, sxt = _wgrad_operands(M, N, K, seed=40 + M)
+    main = np.random.default_rng(M).standard_normal((N, K)).astype(np.float32)
+    got = oracle.gemm_wgrad_accumulate(main, qdyt, sdyt, qxt, sxt, M)
+    want = main.astype(np.float64) + brute_wgrad(qdyt, sdyt, qxt, sxt)
+    assert _close(got, want)
+    rows = np.array([3, 0, N - 1])
+    assert np.array_equal(oracle.gemm_wgrad_accumulate(main, qdyt, sdyt, qxt, sxt, M, rows=rows), got[rows])
+
+
+def test_wgrad_accumulate_twice_from_zero_doubles(oracle_lib):
+    qdyt, sdyt, qxt, sxt = _wgrad_operands(130, 128, 256, seed=77)
+    zero = np.zeros((128, 256), dtype=np.float32)
+    once = oracle.gemm_wgrad_accumulate(zero, qdyt, sdyt, qxt, sxt, 130)
+    assert np.array_equal(once, oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, 130))
+    # dW values are FP64 sums; adding a float32-rounded copy of dW back is what a
+    # second call does to an FP32 main gradient, and doubling is exact in FP64
+    assert np.array_equal(2.0 * once, once + once)
+    twice = oracle.gemm_wgrad_accumulate(once.astype(np.float32), qdyt, sdyt, qxt, sxt, 130)
+    assert _close(twice, 2.0 * once, rtol=1e-7)
