@@ -185,11 +185,12 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     else
         ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN / Cfg::CLUSTER,
                             CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, 1,
+    // scales: one box holds SGROUP chunks (rows) of 128 (A) or BN (B) scales
+    ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, Cfg::SGROUP,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (Cfg::SB_VEC)
-        ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sb, p.gn, nc, p.ld_sb * 4, Cfg::BN, 1,
-                            CU_TENSOR_MAP_SWIZZLE_NONE);
+        ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sb, p.gn, nc, p.ld_sb * 4, Cfg::BN,
+                            Cfg::SGROUP, CU_TENSOR_MAP_SWIZZLE_NONE);
     else
         tmSB = tmSA;  // unused in scalar mode
     if (Cfg::EPI == EPI_F32_ADD)

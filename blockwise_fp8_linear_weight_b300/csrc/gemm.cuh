@@ -18,12 +18,17 @@
 //   operand ring (STAGES deep): the A tile 128x128 and the B tile (BNx128
 //     K-major, or 128-column boxes of an MN-major operand) of one chunk; a
 //     stage is handed back to the producer by the MMA completion alone;
-//   scale ring (SSTAGES deep): the chunk's 128 A scales and, in vector mode,
-//     its BN B scales; a stage is handed back by the promotion warps.
+//   scale ring (SSTAGES deep): the scales of a group of SGROUP chunks of one
+//     tile (128 A scales per chunk; BN B scales per chunk in vector mode, one
+//     per 128 columns in scalar mode); a stage is handed back by the promotion
+//     warps once per group, so that their per-chunk work holds one barrier
+//     wait (the TMEM buffer) instead of two.
 // Warp roles:
-//   warp 0      TMA producer of both rings;
+//   warp 0      TMA producer of the operand ring;
 //   warp 1      allocates TMEM; one thread issues 4 tcgen05.mma (K = 32 each)
 //               per chunk into one of two TMEM accumulators of BN columns;
+//   warp 2      producer of the scale ring (TMA for the per-row and per-column
+//               scales; plain loads for the scalar B scales);
 //   warps 4..11 promotion: warp w owns TMEM lanes 32 (w%4) .. +31 (output rows)
 //               and BN/2 columns; per chunk it reads the partial sums with
 //               tcgen05.ld (two loads in flight per wait), releases the TMEM
@@ -64,7 +69,8 @@ struct GemmConfig {
     static constexpr int BN = BN_;
     static constexpr int BK = 128;
     static constexpr int STAGES = STAGES_;
-    static constexpr int SSTAGES = 8;
+    static constexpr int SGROUP = 4;   // chunks per scale stage
+    static constexpr int SSTAGES = 2;  // scale stages
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
     // epilogue: EPI_BF16_TMA stages BF16 tiles in shared memory and stores them
@@ -93,10 +99,11 @@ struct GemmConfig {
     static constexpr int TMEM_COLS = 512;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
-    static constexpr int SA_BYTES = BM * 4;
-    static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;
+    static constexpr int SA_BYTES = BM * 4;               // A scales of one chunk
+    static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;  // vector-mode B scales of one chunk
+    static constexpr int SBS_PER_CHUNK = BN / 128;        // scalar-mode B scales of one chunk
     static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
-    static constexpr uint32_t SC_TX = SA_BYTES + SB_BYTES;
+    static constexpr uint32_t SC_TX = SGROUP * (SA_BYTES + SB_BYTES);  // TMA bytes of one scale stage
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
     // (64 BF16 or 32 FP32 columns; 4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
@@ -106,8 +113,9 @@ struct GemmConfig {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_OUT = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SA = OFF_OUT + STAGE_OUT_BYTES;
-    static constexpr int OFF_SB = OFF_SA + SSTAGES * SA_BYTES;
-    static constexpr int OFF_BAR = OFF_SB + SSTAGES * SB_BYTES;
+    static constexpr int OFF_SB = OFF_SA + SSTAGES * SGROUP * SA_BYTES;
+    static constexpr int OFF_SBS = OFF_SB + SSTAGES * SGROUP * SB_BYTES;
+    static constexpr int OFF_BAR = (OFF_SBS + SSTAGES * SGROUP * SBS_PER_CHUNK * 4 + 7) / 8 * 8;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * SSTAGES + 2 * NBUF + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -171,6 +179,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t* sOut = smem + Cfg::OFF_OUT;
     float* sSA = reinterpret_cast<float*>(smem + Cfg::OFF_SA);
     float* sSB = reinterpret_cast<float*>(smem + Cfg::OFF_SB);
+    float* sSBs = reinterpret_cast<float*>(smem + Cfg::OFF_SBS);  // scalar-mode B scales
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* full = bars;                       // operand stage landed (TMA)
     uint64_t* empty = full + Cfg::STAGES;        // operand stage consumed (MMA commit)
@@ -266,16 +275,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     tma_load_2d(sB + s * Cfg::B_BYTES, &tmB, &full[s], c * Cfg::BK, n0);
                 }
-                const int ss = g % Cfg::SSTAGES;
-                const uint32_t sph = (g / Cfg::SSTAGES) & 1;
-                if (!mbar_wait(&sempty[ss], sph ^ 1, abort_flag, args.status)) {
-                    ++issued;  // the operand copies of chunk g are in flight
-                    break;
-                }
-                mbar_arrive_expect_tx(&sfull[ss], Cfg::SC_TX);
-                tma_load_2d(sSA + ss * Cfg::BM, &tmSA, &sfull[ss], m0, c);
-                if (Cfg::SB_VEC)
-                    tma_load_2d(sSB + ss * Cfg::BN, &tmSB, &sfull[ss], n0, c);
                 ++issued;
                 if (++c == nc) {
                     c = 0;
@@ -288,12 +287,58 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             volatile int never = 0;
             for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g)
                 mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status);
-            const int sissued = issued;  // scale copies issued (the last one may be missing on abort)
-            for (int g = sissued - Cfg::SSTAGES < 0 ? 0 : sissued - Cfg::SSTAGES; g < sissued; ++g) {
-                // an abort between the operand and the scale copy of chunk g leaves sfull
-                // without that phase; its wait then ends at the time limit
-                mbar_wait(&sfull[g % Cfg::SSTAGES], (g / Cfg::SSTAGES) & 1, &never, args.status);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- scale producer
+        // Groups of SGROUP chunks of one tile (the last group of a tile may be
+        // shorter: TMA fills the rows past the last chunk with zeros, and the
+        // promotion warps never read them).
+        constexpr int NSBS = Cfg::SGROUP * Cfg::SBS_PER_CHUNK;
+        static_assert(NSBS <= 32, "one lane per scalar B scale of a group");
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < my_tiles && ok; ++t) {
+            int m0, n0;
+            tile_origin<Cfg>(args, t, m0, n0);
+            for (int c0 = 0; c0 < nc; c0 += Cfg::SGROUP) {
+                const int qs = issued % Cfg::SSTAGES;
+                const uint32_t qph = (issued / Cfg::SSTAGES) & 1;
+                // lane 0 waits and the warp follows its verdict, so that no lane can
+                // leave the loop while the others reach the __syncwarp below
+                int ready = 1;
+                if (lane == 0)
+                    ready = mbar_wait(&sempty[qs], qph ^ 1, abort_flag, args.status) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (!Cfg::SB_VEC) {
+                    // lane i: chunk c0 + i / SBS_PER_CHUNK, 128-column block i % SBS_PER_CHUNK
+                    if (lane < NSBS) {
+                        const int c = c0 + lane / Cfg::SBS_PER_CHUNK;
+                        const int col = n0 + (lane % Cfg::SBS_PER_CHUNK) * 128;
+                        float v = 0.0f;
+                        if (c < nc && col < args.gn)
+                            v = __ldg(args.sb_scalar + static_cast<int64_t>(col >> 7) * args.sb_col_stride +
+                                      static_cast<int64_t>(c) * args.sb_chunk_stride);
+                        sSBs[qs * NSBS + lane] = v;
+                    }
+                    __syncwarp();  // the stores above happen before lane 0's arrive (release)
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sfull[qs], Cfg::SC_TX);
+                    tma_load_2d(sSA + qs * Cfg::SGROUP * Cfg::BM, &tmSA, &sfull[qs], m0, c0);
+                    if (Cfg::SB_VEC)
+                        tma_load_2d(sSB + qs * Cfg::SGROUP * Cfg::BN, &tmSB, &sfull[qs], n0, c0);
+                }
+                ++issued;
             }
+        }
+        // no copy may still be landing in shared memory at exit
+        if (lane == 0) {
+            volatile int never = 0;
+            for (int q = issued - Cfg::SSTAGES < 0 ? 0 : issued - Cfg::SSTAGES; q < issued; ++q)
+                mbar_wait(&sfull[q % Cfg::SSTAGES], (q / Cfg::SSTAGES) & 1, &never, args.status);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -371,45 +416,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int i = 0; i < CPW / 2; ++i)
             acc[i] = 0;
 
-        // Scalar-mode B scale (one value per warp and chunk), fetched two chunks
-        // ahead by a cursor that walks the chunks in order; the tile origin is
-        // recomputed once per tile, not per chunk.
-        int sb_t = 0, sb_c_idx = 0, sb_m0 = 0, sb_n0 = 0;
-        tile_origin<Cfg>(args, 0, sb_m0, sb_n0);
-        auto next_sb = [&]() -> float {
-            float v = 0.0f;
-            if (!Cfg::SB_VEC && sb_t < my_tiles) {
-                const int col = sb_n0 + half * CPW;
-                if (col < args.gn)
-                    v = __ldg(args.sb_scalar + static_cast<int64_t>(col >> 7) * args.sb_col_stride +
-                              static_cast<int64_t>(sb_c_idx) * args.sb_chunk_stride);
-                if (++sb_c_idx == nc) {
-                    sb_c_idx = 0;
-                    ++sb_t;
-                    tile_origin<Cfg>(args, sb_t, sb_m0, sb_n0);
-                }
-            }
-            return v;
-        };
-        float sb0 = next_sb();
-        float sb1 = next_sb();
-
         int t = 0, c = 0, m0 = 0, n0 = 0;
         tile_origin<Cfg>(args, 0, m0, n0);
+        int qs = 0, gi = 0;  // scale stage and chunk index within its group
+        uint32_t qph = 0;
         for (int g = 0; g < my_chunks; ++g) {
-            const int ss = g % Cfg::SSTAGES;
-            const uint32_t sph = (g / Cfg::SSTAGES) & 1;
             const int b = g % Cfg::NBUF;
             const uint32_t bph = (g / Cfg::NBUF) & 1;
-            const float sb_c = sb0;
-            sb0 = sb1;
-            sb1 = next_sb();
-            if (!mbar_wait(&sfull[ss], sph, abort_flag, args.status))
+            if (gi == 0 && !mbar_wait(&sfull[qs], qph, abort_flag, args.status))
                 break;
             if (!mbar_wait(&tfull[b], bph, abort_flag, args.status))
                 break;
             tc_fence_after_sync();
-            const float sa = sSA[ss * Cfg::BM + row];
+            const int slot = qs * Cfg::SGROUP + gi;  // this chunk's row of the scale stage
+            const float sa = sSA[slot * Cfg::BM + row];
+            const float sb_c = Cfg::SB_VEC ? 0.0f
+                                           : sSBs[slot * Cfg::SBS_PER_CHUNK + (half * CPW) / 128];
             const uint64_t sa2 = pack_f32x2(sa, sa);
             const float sc = sa * sb_c;
             const uint64_t sc2 = pack_f32x2(sc, sc);
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (Cfg::SB_VEC) {
                     // per-column scales: broadcast 16-byte shared-memory reads (two column pairs each)
                     const ulonglong2* sbv =
-                        reinterpret_cast<const ulonglong2*>(sSB + ss * Cfg::BN + half * CPW + j * LW);
+                        reinterpret_cast<const ulonglong2*>(sSB + slot * Cfg::BN + half * CPW + j * LW);
 #pragma unroll
                     for (int i = 0; i < LW / 4; ++i) {
                         const ulonglong2 v = sbv[i];
@@ -443,10 +465,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ffma2(a[i], p[i], sc2);
                 }
             }
-            // this warp is done with the chunk's scales
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sempty[ss]);
+            // the group's last chunk (or the tile's): this warp is done with the stage
+            if (gi == Cfg::SGROUP - 1 || c == nc - 1) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sempty[qs]);
+                gi = 0;
+                if (++qs == Cfg::SSTAGES) {
+                    qs = 0;
+                    qph ^= 1;
+                }
+            } else {
+                ++gi;
+            }
 
             if (++c == nc) {
                 // ------------------------------------------------ BF16 epilogue of tile t
