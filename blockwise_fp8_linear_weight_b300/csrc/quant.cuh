@@ -62,6 +62,50 @@ __device__ __forceinline__ TileScale tile_scale(float amax)
     return t;
 }
 
+// Tile scales without a division: for a BF16 amax = (1 + i/128) * 2^(E - 127)
+// (biased exponent E, 7-bit mantissa i) and 448 = 1.75 * 2^8,
+//   amax / 448 = ((1 + i/128) / 1.75) * 2^(E - 135),
+// and rounding commutes with the power-of-two factor whenever the result is a
+// normal binary32 number, which holds for E >= 10. So s = T1[i] * 2^(E - 135)
+// with T1[i] = RN((1 + i/128) / 1.75), and y = RN(1 / sp) = T2[i] * 2^-(E - 135 + P)
+// with T2[i] = RN(1 / T1[i]) and P = 64 for pre-scaled tiles: two table reads
+// and integer additions to the exponent field. Each CTA fills the 128-entry
+// tables with IEEE divisions when it starts; zero and tiny maxima (E < 10,
+// scales that are zero or subnormal) take tile_scale's divisions.
+struct ScaleTables {
+    uint32_t t1[128];  // bits of RN((1 + i/128) / 1.75)
+    uint32_t t2[128];  // bits of RN(1 / T1[i])
+};
+
+__device__ __forceinline__ void init_scale_tables(ScaleTables& t)
+{
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const float q = __fdiv_rn(1.0f + static_cast<float>(i) * 0.0078125f, 1.75f);
+        t.t1[i] = __float_as_uint(q);
+        t.t2[i] = __float_as_uint(__frcp_rn(q));
+    }
+}
+
+__device__ __forceinline__ TileScale tile_scale_tab(float amax, const ScaleTables& t)
+{
+    const uint32_t ab = __float_as_uint(amax);
+    const int E = static_cast<int>(ab >> 23);
+    if (E < 10)
+        return tile_scale(amax);
+    const uint32_t i = (ab >> 16) & 0x7Fu;
+    const uint32_t t1 = t.t1[i];
+    const uint32_t k = static_cast<uint32_t>(E - 135) << 23;  // exponent offset (wraps for E < 135)
+    const uint32_t sbits = t1 + k;
+    const bool scaled = (sbits >> 23) < 67u;  // s < 2^-60
+    const uint32_t kp = scaled ? k + (64u << 23) : k;
+    TileScale r;
+    r.s = __uint_as_float(sbits);
+    r.pre = scaled ? 0x1p64f : 1.0f;
+    r.sp = __uint_as_float(t1 + kp);
+    r.y = __uint_as_float(t.t2[i] - kp);
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Packed form used by the kernels: two values per 64-bit register pair, so the
 // five quotient steps (one product, two Markstein corrections) are five packed
@@ -74,6 +118,19 @@ struct PairScale {
     uint64_t pre;  // {pre_lo, pre_hi}
     bool scaled;   // some lane has pre != 1
 };
+
+// One scale for both lanes, from a broadcast (y, signed sp): sp > 0 marks a
+// pre-scaled tile, and the FMA operand is -|sp| either way.
+__device__ __forceinline__ PairScale pair_scale_bcast(float y, float sp_signed)
+{
+    PairScale p;
+    const float ns = -fabsf(sp_signed);
+    p.ns = pack_f32x2(ns, ns);
+    p.y = pack_f32x2(y, y);
+    p.pre = pack_f32x2(0x1p64f, 0x1p64f);
+    p.scaled = sp_signed > 0.0f;
+    return p;
+}
 
 __device__ __forceinline__ PairScale pair_scale(const TileScale& lo, const TileScale& hi)
 {
@@ -206,9 +263,9 @@ __device__ __forceinline__ void column_encode(const uint32_t (*tile)[64], int qu
     }
 }
 
-__device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t (*part)[64], int64_t cb, int64_t rb,
-                                            uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ st,
-                                            int64_t ldst)
+__device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t (*part)[64], const ScaleTables& tab,
+                                            int64_t cb, int64_t rb, uint8_t* __restrict__ qt, int64_t ldqt,
+                                            float* __restrict__ st, int64_t ldst)
 {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -223,7 +280,7 @@ __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t
     part[quarter][cw] = m & 0x7FFF7FFFu;
     __syncthreads();
     m = bf16x2_max(bf16x2_max(part[0][cw], part[1][cw]), bf16x2_max(part[2][cw], part[3][cw]));
-    const TileScale s0 = tile_scale(bf16_lo(m)), s1 = tile_scale(bf16_hi(m));
+    const TileScale s0 = tile_scale_tab(bf16_lo(m), tab), s1 = tile_scale_tab(bf16_hi(m), tab);
     const PairScale ps = pair_scale(s0, s1);
 
     uint32_t c0[8], c1[8];
@@ -279,6 +336,7 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
     __shared__ __align__(8) uint64_t full[2];
     __shared__ __align__(16) uint32_t part[4][64];
     __shared__ uint32_t red[8];
+    __shared__ ScaleTables stab;
     __shared__ int abort_flag;
     const int tid = threadIdx.x;
     const int sub = tid & 15;
@@ -295,6 +353,7 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         tma_load_2d(tiles + (i & 1) * kQuantTileBytes, &tmX, bar, static_cast<int32_t>(cb * 128),
                     static_cast<int32_t>(rb * 128));
     };
+    init_scale_tables(stab);
     if (tid == 0) {
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
@@ -347,28 +406,30 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
                 m[0] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
                 m[0] = bf16x2_max(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
             }
-            const TileScale mine = tile_scale(fmaxf(bf16_lo(m[0]), bf16_hi(m[0])));  // tile (sub >> 1)
+            const TileScale mine = tile_scale_tab(fmaxf(bf16_lo(m[0]), bf16_hi(m[0])), stab);  // tile sub >> 1
             const int lane = tid & 31;
+            const int64_t r0 = rb * 128 + (tid >> 4);  // the thread's row for j = 0
+            // lanes 2j store tile j's scale (rows r0 - ... + 16 j of their half-warp)
+            if ((sub & 1) == 0 && r0 + 16 * (sub >> 1) < a.R)
+                a.s[cb * a.lds + r0 + 16 * (sub >> 1)] = mine.s;
+            const float bc_sp = mine.pre != 1.0f ? mine.sp : -mine.sp;  // sign carries the pre-scaling flag
+            const int rows_left = static_cast<int>(a.R - r0 > 128 ? 128 : a.R - r0);
+            uint8_t* qrow = a.q + r0 * a.ldq + cb * 128 + sub * 8;
+            const int64_t qstep = 16 * a.ldq;
 #pragma unroll 2
             for (int j = 0; j < 8; ++j) {
                 const int src = (lane & 16) | (2 * j);
-                TileScale ts;
-                ts.s = __shfl_sync(0xffffffffu, mine.s, src);
-                ts.pre = __shfl_sync(0xffffffffu, mine.pre, src);
-                ts.sp = __shfl_sync(0xffffffffu, mine.sp, src);
-                ts.y = __shfl_sync(0xffffffffu, mine.y, src);
-                const int row = (tid >> 4) + 16 * j;
-                const int64_t gr = rb * 128 + row;
-                if (gr < a.R) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
-                    *reinterpret_cast<uint2*>(a.q + gr * a.ldq + cb * 128 + sub * 8) = codes8(v, pair_scale(ts, ts));
-                    if (sub == 0)
-                        a.s[cb * a.lds + gr] = ts.s;
+                const PairScale ps = pair_scale_bcast(__shfl_sync(0xffffffffu, mine.y, src),
+                                                      __shfl_sync(0xffffffffu, bc_sp, src));
+                if (16 * j < rows_left) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4]);
+                    *reinterpret_cast<uint2*>(qrow) = codes8(v, ps);
                 }
+                qrow += qstep;
             }
         }
         if (MODE == MODE_COLS || MODE == MODE_DUAL)
-            column_pass(tile, part, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+            column_pass(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
         if (MODE == MODE_WEIGHT) {
             uint32_t m = 0;
 #pragma unroll
@@ -384,7 +445,7 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
 #pragma unroll
             for (int k = 1; k < 8; ++k)
                 m = bf16x2_max(m, red[k]);
-            const TileScale ts = tile_scale(fmaxf(bf16_lo(m), bf16_hi(m)));
+            const TileScale ts = tile_scale_tab(fmaxf(bf16_lo(m), bf16_hi(m)), stab);
             const PairScale ps = pair_scale(ts, ts);
             auto encode = [&](auto scaled) {
 #pragma unroll 2

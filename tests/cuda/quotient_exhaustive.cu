@@ -9,6 +9,9 @@
 //     x / s, counted where |x / s| >= 2^-12 (below 2^-10 every code is a
 //     signed zero).
 // For an all-zero tile (amax = 0) the definition's quotient is x itself.
+// The tile scale comes from the kernels' table path (tile_scale_tab), which is
+// also compared field by field with the division-based tile_scale for every
+// amax (a mismatch there counts once per value).
 #include <cstdint>
 #include <cstdio>
 #include <cuda_runtime.h>
@@ -17,9 +20,23 @@
 
 __global__ void check(unsigned long long* pairs, unsigned long long* bad, unsigned* first)
 {
+    __shared__ bfp8::ScaleTables tab;
+    bfp8::init_scale_tables(tab);
+    __syncthreads();
     const unsigned ab = blockIdx.y;  // amax bit pattern (0 .. largest finite)
     const float amax = __uint_as_float(ab << 16);
-    const bfp8::TileScale ts = bfp8::tile_scale(amax);
+    const bfp8::TileScale ts = bfp8::tile_scale_tab(amax, tab);
+    const bfp8::TileScale td = bfp8::tile_scale(amax);
+    if (blockIdx.x == 0 && threadIdx.x == 0 &&
+        (__float_as_uint(ts.s) != __float_as_uint(td.s) || __float_as_uint(ts.sp) != __float_as_uint(td.sp) ||
+         __float_as_uint(ts.y) != __float_as_uint(td.y) || ts.pre != td.pre)) {
+        const unsigned long long k = atomicAdd(bad, 1ull);
+        if (k < 4) {
+            first[3 * k] = 0xFFFFFFFFu;  // marks a scale mismatch
+            first[3 * k + 1] = ab;
+            first[3 * k + 2] = __float_as_uint(ts.s);
+        }
+    }
     const bfp8::PairScale ps = bfp8::pair_scale(ts, ts);
     unsigned long long n = 0;
     for (unsigned xb = blockIdx.x * blockDim.x + threadIdx.x; xb < 65536u; xb += gridDim.x * blockDim.x) {
