@@ -52,7 +52,8 @@ def parse():
     p.add_argument("--no-extras", action="store_true",
                    help="skip the side measurements (cuBLAS BF16 comparator, FP32-accumulating wgrad, "
                         "weight-quantisation reuse)")
-    p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 256], help="GEMM tile width (0: automatic)")
+    p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 192, 256],
+                   help="GEMM tile width (0: automatic)")
     p.add_argument("--gemm-cluster", type=int, default=0, choices=[0, 1, 2], help="GEMM CTAs per cluster (0: automatic)")
     p.add_argument("--gemm-promo-warps", type=int, default=0, choices=[0, 8, 16],
                    help="GEMM promotion warps per CTA (0: library default)")

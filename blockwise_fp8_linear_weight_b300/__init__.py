@@ -235,10 +235,10 @@ def last_device_status() -> int:
 
 
 def set_gemm_tile_n(tile_n: int) -> int:
-    """GEMM output tile width: 0 (automatic), 128 or 256. Returns the previous value."""
+    """GEMM output tile width: 0 (automatic), 128, 192 or 256. Returns the previous value."""
     rc = load_library().bfp8_set_gemm_tile_n(int(tile_n))
     if rc < 0:
-        raise ValueError("tile_n must be 0, 128 or 256")
+        raise ValueError("tile_n must be 0, 128, 192 or 256")
     return rc
 
 

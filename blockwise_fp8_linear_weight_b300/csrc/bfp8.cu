@@ -270,6 +270,11 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
         tn = 256;
     if (tn == 128)
         return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
+    if constexpr (!B_MN) {
+        // 192-wide tiles: 12 promotion warps of 64 columns (one TMEM load per chunk each)
+        if (tn == 192)
+            return run_gemm<GemmConfig<192, 4, B_MN, SB_VEC, 1, EPI_BF16_TMA, 12>>(p, status, stream, dev);
+    }
     int cl = g_cluster.load(std::memory_order_relaxed);
     if (cl == 0)
         cl = 1;  // measured: multicast halves L2 traffic but the path is not L2-bound
@@ -630,7 +635,7 @@ extern "C" int bfp8_set_gemm_cluster(int cluster)
 
 extern "C" int bfp8_set_gemm_tile_n(int tile_n)
 {
-    if (tile_n != 0 && tile_n != 128 && tile_n != 256)
+    if (tile_n != 0 && tile_n != 128 && tile_n != 192 && tile_n != 256)
         return BFP8_EINVAL;
     return g_tile_n.exchange(tile_n);
 }

@@ -91,17 +91,21 @@ struct GemmConfig {
     static constexpr int CPW = BN / GROUPS;  // output columns per promotion warp
     static constexpr int LW = CPW == 64 && PW_ == 16 ? 32 : 64;  // columns per TMEM load
     static constexpr int THREADS = 128 + 32 * PROMO_WARPS;
-    static constexpr bool REG_SPLIT = (BN == 256);
+    static constexpr bool REG_SPLIT = (BN >= 192);
     // TMEM accumulator buffers: as many BN-column buffers as the 512 columns hold
     // (2 at BN = 256, 4 at BN = 128), i.e. that many chunks in flight between the
     // MMA issuer and the promotion warps
     static constexpr int NBUF = 512 / BN;
+    // TMEM columns between buffers: 192-wide accumulators start on 256-column boundaries
+    static constexpr int BUF_STRIDE = BN == 192 ? 256 : BN;
     static constexpr int TMEM_COLS = 512;
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SA_BYTES = BM * 4;               // A scales of one chunk
     static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;  // vector-mode B scales of one chunk
-    static constexpr int SBS_PER_CHUNK = BN / 128;        // scalar-mode B scales of one chunk
+    // scalar-mode B scales of one chunk: the 128-column blocks a tile touches (a
+    // 192-wide tile at a multiple of 192 touches two)
+    static constexpr int SBS_PER_CHUNK = BN == 128 ? 1 : 2;
     static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
     static constexpr uint32_t SC_TX = SGROUP * (SA_BYTES + SB_BYTES);  // TMA bytes of one scale stage
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
@@ -119,16 +123,17 @@ struct GemmConfig {
     static constexpr int NUM_BARS = 2 * STAGES + 2 * SSTAGES + 2 * NBUF + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-    static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
+    static_assert(BN == 128 || BN == 192 || BN == 256, "BN must be 128, 192 or 256");
+    static_assert(BN != 192 || (!B_MN && CPW == 64), "192-wide tiles: K-major B, 64 columns per promotion warp");
     static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN == 256), "clusters of 2 with 256-wide tiles only");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     // registers per thread at launch (65536 / THREADS, rounded down to a multiple of 8)
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
     // setmaxnreg split between the producer/MMA warpgroup and the two promotion
     // warpgroups (chosen so that neither side spills on its hot path)
-    static constexpr int REG_LOW = PW_ == 16 ? 32 : (SB_VEC ? 64 : 56);
-    static constexpr int REG_HIGH = PW_ == 16 ? 112 : (SB_VEC ? 216 : 224);
-    static_assert(PW_ == 8 || PW_ == 16, "8 or 16 promotion warps");
+    static constexpr int REG_LOW = PW_ == 16 ? 32 : (PW_ == 12 ? 56 : (SB_VEC ? 64 : 56));
+    static constexpr int REG_HIGH = PW_ == 16 ? 112 : (PW_ == 12 ? 152 : (SB_VEC ? 216 : 224));
+    static_assert(PW_ == 8 || PW_ == 12 || PW_ == 16, "8, 12 or 16 promotion warps");
     static_assert(!REG_SPLIT || 128 * REG_LOW + 32 * PW_ * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
 };
 
@@ -313,10 +318,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 if (!Cfg::SB_VEC) {
-                    // lane i: chunk c0 + i / SBS_PER_CHUNK, 128-column block i % SBS_PER_CHUNK
+                    // lane i: chunk c0 + i / SBS_PER_CHUNK, the tile's 128-column block i % SBS_PER_CHUNK
                     if (lane < NSBS) {
                         const int c = c0 + lane / Cfg::SBS_PER_CHUNK;
-                        const int col = n0 + (lane % Cfg::SBS_PER_CHUNK) * 128;
+                        const int col = ((n0 >> 7) + lane % Cfg::SBS_PER_CHUNK) * 128;
                         float v = 0.0f;
                         if (c < nc && col < args.gn)
                             v = __ldg(args.sb_scalar + static_cast<int64_t>(col >> 7) * args.sb_col_stride +
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     bph ^= 1;
                     d_tmem = tmem_base;
                 } else {
-                    d_tmem += Cfg::BN;
+                    d_tmem += Cfg::BUF_STRIDE;
                 }
             }
             // all issued MMAs must be complete before TMEM is released
@@ -430,13 +435,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after_sync();
             const int slot = qs * Cfg::SGROUP + gi;  // this chunk's row of the scale stage
             const float sa = sSA[slot * Cfg::BM + row];
-            const float sb_c = Cfg::SB_VEC ? 0.0f
-                                           : sSBs[slot * Cfg::SBS_PER_CHUNK + (half * CPW) / 128];
+            const float sb_c =
+                Cfg::SB_VEC ? 0.0f
+                            : sSBs[slot * Cfg::SBS_PER_CHUNK + ((n0 + half * CPW) >> 7) - (n0 >> 7)];
             const uint64_t sa2 = pack_f32x2(sa, sa);
             const float sc = sa * sb_c;
             const uint64_t sc2 = pack_f32x2(sc, sc);
             const uint32_t t_base =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BN + half * CPW;
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BUF_STRIDE + half * CPW;
             constexpr int LW = Cfg::LW;
 #pragma unroll
             for (int j = 0; j < CPW / LW; ++j) {

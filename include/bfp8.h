@@ -148,8 +148,10 @@ const char* bfp8_status_string(int status);
 int bfp8_last_device_status(void* stream);
 
 /* Tuning knob for the GEMMs' output tile width: 0 = automatic (default),
- * 128 or 256 columns. Returns the previous setting, or BFP8_EINVAL. Applies
- * to later calls from every thread. */
+ * 128, 192 or 256 columns (192 applies to the forward and weight-gradient
+ * GEMMs, whose B operand is K-major; the input-gradient GEMM then uses 256).
+ * Returns the previous setting, or BFP8_EINVAL. Applies to later calls from
+ * every thread. */
 int bfp8_set_gemm_tile_n(int tile_n);
 
 /* Tuning knob for the 256-wide GEMM tiles: 0 = automatic (default, currently

@@ -22,12 +22,13 @@ pytestmark = pytest.mark.gpu
 TILE = 128
 
 
-@pytest.fixture(params=[(128, 1, 8), (256, 1, 8), (256, 2, 8), (256, 1, 16)],
+@pytest.fixture(params=[(128, 1, 8), (192, 1, 8), (256, 1, 8), (256, 2, 8), (256, 1, 16)],
                 ids=lambda p: f"tileN{p[0]}-cluster{p[1]}-warps{p[2]}")
 def tile_n(request):
-    """Every tile configuration: 128-wide tiles, 256-wide tiles one CTA each, 256-wide
-    tiles in clusters of two CTAs sharing B through multicast, and 256-wide tiles
-    with 16 promotion warps."""
+    """Every tile configuration: 128-wide tiles, 192-wide tiles with 12 promotion warps
+    (forward and weight gradient; the input gradient then runs 256-wide), 256-wide
+    tiles one CTA each, 256-wide tiles in clusters of two CTAs sharing B through
+    multicast, and 256-wide tiles with 16 promotion warps."""
     tn, cl, pw = request.param
     prev_t = bfp8.set_gemm_tile_n(tn)
     prev_c = bfp8.set_gemm_cluster(cl)
