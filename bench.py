@@ -479,7 +479,10 @@ def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_t
         BF16 on its RTX 5090s);
       wgrad_fp32_acc: the weight-gradient GEMM accumulating into an FP32 main gradient;
       weight_quant_reuse: the training step of a micro-batch after the first, W's codes reused
-        (five kernels per linear)."""
+        (five kernels per linear);
+      muonh: one MuonH optimizer step on every linear's weight (FP32 master copy, N(0,1)
+        gradient): the library's normalise and apply kernels around five BF16 Newton-Schulz
+        iterations (cuBLAS GEMMs); rate = the iterations' GEMM FLOP over the whole update."""
     def timed(fn, n):
         for _ in range(3):
             fn()
@@ -540,6 +543,24 @@ def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_t
     out["weight_quant_reuse"] = {"tflops": round(work.flops / (ms_reuse / 1e3) / 1e12, 1),
                                  "ms_per_step": round(ms_reuse, 4),
                                  "kernels_per_step": 5 * len(layers)}
+    # MuonH: every linear's weight gets one optimizer step per iteration
+    mw = [(torch.randn((l.N, l.K), device=dev) * 0.02).float() for l in work.linears]
+    mg = [torch.randn((l.N, l.K), device=dev) for l in work.linears]
+    radii = [float(w.norm()) for w in mw]
+
+    def muonh_step():
+        for w, g, r in zip(mw, mg, radii):
+            bfp8.muonh_update(w, g, 0.02, r)
+
+    mu_steps = max(3, min(steps, 20))
+    ms_mu = timed(muonh_step, mu_steps)
+    ns_flops = 0
+    for l in work.linears:
+        r_, c_ = min(l.N, l.K), max(l.N, l.K)
+        ns_flops += 5 * (4 * r_ * r_ * c_ + 2 * r_ ** 3)
+    out["muonh"] = {"ms_per_update_all_linears": round(ms_mu, 4),
+                    "ns_gemm_tflops": round(ns_flops / (ms_mu / 1e3) / 1e12, 1),
+                    "steps": mu_steps}
     out["steps_each"] = steps
     return out
 

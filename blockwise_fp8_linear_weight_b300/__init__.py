@@ -15,6 +15,8 @@ Entry points (same names as the C ABI):
   fp8_block_gemm_dgrad(qdy, sdy, qw, sw)    -> dx [M, K] bf16
   fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M) -> dw [N, K] bf16
   fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad): main_grad [N, K] f32 += dW
+MuonH (one optimizer step for one weight matrix):
+  muonh_update(w, g, lr, radius)  # w FP32 in place; see muonh_update's docstring
 Scale tensors are allocated with a row stride rounded up to 4 elements so that
 the GEMMs' TMA loads see 16-byte rows; the returned tensors are views of the
 valid columns.
@@ -69,6 +71,9 @@ def load_library(path: str = LIB_PATH):
         "bfp8_set_gemm_tile_n": [c_int],
         "bfp8_set_gemm_cluster": [c_int],
         "bfp8_set_gemm_promo_warps": [c_int],
+        "muonh_partials_len": [ctypes.POINTER(c_int)],
+        "muonh_normalize": [p, i64, i64, i64, p, i64, p, ctypes.c_float, p],
+        "muonh_apply": [p, i64, p, i64, i64, i64, p, ctypes.c_float, ctypes.c_float, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -338,3 +343,68 @@ class BlockwiseFP8Linear:
             return self.dx, self.main_grad
         fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw)
         return self.dx, self.dw
+
+
+# ----------------------------------------------------------------------- MuonH
+# Quintic Newton-Schulz coefficients of the public Muon optimizer (K. Jordan et
+# al., "Muon: an optimizer for hidden layers in neural networks", 2024); the
+# Puro-2B pages name MuonH but give no coefficients.
+MUON_NS_COEFFS = (3.4445, -4.7750, 2.0315)
+
+
+def _muonh_partials(device):
+    n = ctypes.c_int(0)
+    _check("muonh_partials_len", load_library().muonh_partials_len(ctypes.byref(n)))
+    return torch.empty(n.value, dtype=torch.float64, device=device)
+
+
+def muonh_normalize(g, x=None, eps: float = 1e-7, partials=None):
+    """x = bf16(g / (|g|_F + eps)) for an FP32 matrix g [rows, cols] (cols % 4 == 0)."""
+    lib = load_library()
+    _req(g, torch.float32, "g")
+    rows, cols = g.shape
+    x = torch.empty((rows, cols), dtype=torch.bfloat16, device=g.device) if x is None else x
+    partials = _muonh_partials(g.device) if partials is None else partials
+    _check("muonh_normalize", lib.muonh_normalize(_ptr(g), rows, cols, g.stride(0), _ptr(x), x.stride(0),
+                                                  _ptr(partials), float(eps), _stream()))
+    return x
+
+
+def muonh_apply(w, u, lr: float, radius: float, partials=None):
+    """w = R (w - a u) / |w - a u|_F in place, a = lr R / |u|_F; w FP32, u BF16, same shape."""
+    lib = load_library()
+    _req(w, torch.float32, "w")
+    _req(u, torch.bfloat16, "u")
+    if u.shape != w.shape:
+        raise ValueError("u must have w's shape")
+    rows, cols = w.shape
+    partials = _muonh_partials(w.device) if partials is None else partials
+    _check("muonh_apply", lib.muonh_apply(_ptr(w), w.stride(0), _ptr(u), u.stride(0), rows, cols,
+                                          _ptr(partials), float(lr), float(radius), _stream()))
+    return w
+
+
+def newton_schulz_bf16(x, steps: int = 5, coeffs=MUON_NS_COEFFS):
+    """Quintic Newton-Schulz iterations X <- a X + (b A + c A^2) X, A = X X^T, on the
+    orientation with fewer rows; plain BF16 GEMMs with FP32 accumulation (cuBLAS)."""
+    a, b, c = coeffs
+    t = x.shape[0] > x.shape[1]
+    if t:
+        x = x.t()
+    for _ in range(steps):
+        A = x @ x.t()
+        B = torch.addmm(A, A, A, beta=b, alpha=c)
+        x = torch.addmm(x, B, x, beta=a, alpha=1.0)
+    return x.t() if t else x
+
+
+def muonh_update(w, g, lr: float, radius: float, steps: int = 5, coeffs=MUON_NS_COEFFS, eps: float = 1e-7):
+    """One MuonH step for one weight matrix, in place: w (FP32 [N, K]) moves by a relative
+    step lr along the orthogonalised gradient and is projected back to |w|_F = radius.
+
+    X0 = g / (|g| + eps) (library kernel), U = Newton-Schulz(X0) (BF16 GEMMs),
+    w = radius (w - lr radius U/|U|) / |w - lr radius U/|U|| (library kernels)."""
+    partials = _muonh_partials(w.device)
+    x = muonh_normalize(g, eps=eps, partials=partials)
+    u = newton_schulz_bf16(x, steps, coeffs).contiguous()
+    return muonh_apply(w, u, lr, radius, partials=partials)

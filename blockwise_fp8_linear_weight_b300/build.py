@@ -13,7 +13,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libbfp8.so")
 SOURCES = [os.path.join(CSRC, "bfp8.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant.cuh", "gemm.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "muonh.cuh")] + [
     os.path.join(ROOT, "include", "bfp8.h")]
 
 NVCC_FLAGS = [

@@ -12,6 +12,7 @@
 
 #include "bfp8.h"
 #include "gemm.cuh"
+#include "muonh.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -577,6 +578,76 @@ extern "C" int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, con
     p.gn = K;
     p.gk = M128;
     return dispatch_gemm<false, true, EPI_F32_ADD>(p, static_cast<cudaStream_t>(stream));
+}
+
+// =================================================================== MuonH
+namespace bfp8 {
+namespace {
+// One reduction grid for every MuonH call on a device, so that partial sums
+// written by one kernel are read back by the next one in the same layout.
+int muonh_grid(int dev)
+{
+    return 2 * sm_count(dev);
+}
+}  // namespace
+}  // namespace bfp8
+
+extern "C" int muonh_partials_len(int* n)
+{
+    if (!n)
+        return BFP8_EINVAL;
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    *n = 3 * muonh_grid(dev);
+    return BFP8_OK;
+}
+
+extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, void* x, int64_t ldx,
+                               double* partials, float eps, void* stream)
+{
+    if (rows < 1 || cols < 1)
+        return BFP8_EINVAL;
+    if (cols % 4 || rows > kMaxDim || cols > kMaxDim)
+        return BFP8_ESHAPE;
+    if (!g || !x || !partials || ldg < cols || ldx < cols || !(eps >= 0.0f))
+        return BFP8_EINVAL;
+    if (!aligned(g, 16) || ldg % 4 || !aligned(x, 8) || ldx % 4 || !aligned(partials, 8))
+        return BFP8_EALIGN;
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    const int grid = muonh_grid(dev);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    muonh_sumsq_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials);
+    muonh_scale_bf16_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials, grid, eps,
+                                                          static_cast<uint16_t*>(x), ldx);
+    return launch_status();
+}
+
+extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                           double* partials, float lr, float radius, void* stream)
+{
+    if (rows < 1 || cols < 1)
+        return BFP8_EINVAL;
+    if (cols % 4 || rows > kMaxDim || cols > kMaxDim)
+        return BFP8_ESHAPE;
+    if (!w || !u || !partials || ldw < cols || ldu < cols || !(lr >= 0.0f) || !(radius > 0.0f))
+        return BFP8_EINVAL;
+    if (!aligned(w, 16) || ldw % 4 || !aligned(u, 8) || ldu % 4 || !aligned(partials, 8))
+        return BFP8_EALIGN;
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    const int grid = muonh_grid(dev);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* ub = static_cast<const uint16_t*>(u);
+    muonh_dot3_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials);
+    muonh_apply_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
+    return launch_status();
 }
 
 // =================================================================== misc

@@ -1,0 +1,195 @@
+// MuonH update kernels: the reductions and element-wise passes around the
+// Newton-Schulz orthogonalisation of a gradient.
+//
+// The Puro-2B recipe trains with MuonH (Puro-2B article on en.roboind.com,
+// section "From ordinary learning to effective learning"): the size of each
+// weight update is standardised on top of Muon, and after the update the
+// weight is projected back to a fixed radius; the relative update size is a
+// preset quantity rather than a drift of the weight norm. Read plainly, with
+// U the Newton-Schulz orthogonalisation of the gradient G, a learning rate lr
+// and the radius R (Frobenius norms):
+//   X0    = G / (|G| + eps)                      (muonh_normalize, BF16 out)
+//   U     = Newton-Schulz iterations on X0       (plain BF16 GEMMs)
+//   W'    = W - lr R U / |U|                     (relative update size lr)
+//   W_new = R W' / |W'|                          (back onto the sphere |W| = R)
+// |W'|^2 = |W|^2 - 2 a <W,U> + a^2 |U|^2 with a = lr R / |U|, so one reduction
+// pass over (W, U) gives every norm and one more pass writes W_new.
+//
+// Sums are deterministic: each CTA reduces a fixed set of rows (FP32 within a
+// row segment of a thread, FP64 beyond), warps by a fixed butterfly, CTAs by
+// a fixed loop over the partials; every launch uses the same grid.
+#pragma once
+
+#include <cstdint>
+
+namespace bfp8 {
+
+constexpr int kMuonThreads = 256;
+
+// Sum of three FP64 values over the CTA, in a fixed order; thread 0 returns them.
+__device__ __forceinline__ void block_sum3(double& x, double& y, double& z, double (*sh)[3])
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+        y += __shfl_xor_sync(0xffffffffu, y, o);
+        z += __shfl_xor_sync(0xffffffffu, z, o);
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sh[warp][0] = x;
+        sh[warp][1] = y;
+        sh[warp][2] = z;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        x = y = z = 0.0;
+        for (int w = 0; w < kMuonThreads / 32; ++w) {
+            x += sh[w][0];
+            y += sh[w][1];
+            z += sh[w][2];
+        }
+    }
+}
+
+// Fixed-order total of component k of the CTA partials [nparts][3].
+__device__ __forceinline__ double sum_partials(const double* partials, int nparts, int k)
+{
+    double s = 0.0;
+    for (int i = 0; i < nparts; ++i)
+        s += partials[3 * i + k];
+    return s;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h)
+{
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// partials[blockIdx.x] = (sum of a^2 over the CTA's rows, 0, 0); a FP32 [rows][lda], cols % 4 == 0.
+__global__ void __launch_bounds__(kMuonThreads) muonh_sumsq_kernel(const float* __restrict__ a, int64_t rows,
+                                                                   int64_t cols, int64_t lda,
+                                                                   double* __restrict__ partials)
+{
+    __shared__ double sh[kMuonThreads / 32][3];
+    double acc = 0.0, zero1 = 0.0, zero2 = 0.0;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4* row = reinterpret_cast<const float4*>(a + r * lda);
+        float s = 0.0f;
+        for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
+            const float4 v = row[j];
+            s = fmaf(v.x, v.x, s);
+            s = fmaf(v.y, v.y, s);
+            s = fmaf(v.z, v.z, s);
+            s = fmaf(v.w, v.w, s);
+        }
+        acc += static_cast<double>(s);
+    }
+    block_sum3(acc, zero1, zero2, sh);
+    if (threadIdx.x == 0) {
+        partials[3 * blockIdx.x + 0] = acc;
+        partials[3 * blockIdx.x + 1] = 0.0;
+        partials[3 * blockIdx.x + 2] = 0.0;
+    }
+}
+
+// x = bf16_rn(a / (sqrt(sum of the partials) + eps)); x BF16 [rows][ldx].
+__global__ void __launch_bounds__(kMuonThreads) muonh_scale_bf16_kernel(const float* __restrict__ a, int64_t rows,
+                                                                        int64_t cols, int64_t lda,
+                                                                        const double* __restrict__ partials,
+                                                                        int nparts, float eps,
+                                                                        uint16_t* __restrict__ x, int64_t ldx)
+{
+    __shared__ float inv;
+    if (threadIdx.x == 0)
+        inv = static_cast<float>(1.0 / (sqrt(sum_partials(partials, nparts, 0)) + static_cast<double>(eps)));
+    __syncthreads();
+    const float s = inv;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4* src = reinterpret_cast<const float4*>(a + r * lda);
+        uint2* dst = reinterpret_cast<uint2*>(x + r * ldx);
+        for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
+            const float4 v = src[j];
+            dst[j] = make_uint2(f32x2_to_bf16x2(v.x * s, v.y * s), f32x2_to_bf16x2(v.z * s, v.w * s));
+        }
+    }
+}
+
+// partials[blockIdx.x] = (sum w^2, sum w u, sum u^2) over the CTA's rows; w FP32, u BF16.
+__global__ void __launch_bounds__(kMuonThreads) muonh_dot3_kernel(const float* __restrict__ w, int64_t ldw,
+                                                                  const uint16_t* __restrict__ u, int64_t ldu,
+                                                                  int64_t rows, int64_t cols,
+                                                                  double* __restrict__ partials)
+{
+    __shared__ double sh[kMuonThreads / 32][3];
+    double ww = 0.0, wu = 0.0, uu = 0.0;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4* wr = reinterpret_cast<const float4*>(w + r * ldw);
+        const uint2* ur = reinterpret_cast<const uint2*>(u + r * ldu);
+        float sww = 0.0f, swu = 0.0f, suu = 0.0f;
+        for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
+            const float4 a = wr[j];
+            const uint2 b = ur[j];
+            const float u0 = bf16_to_f32(static_cast<uint16_t>(b.x)), u1 = bf16_to_f32(static_cast<uint16_t>(b.x >> 16));
+            const float u2 = bf16_to_f32(static_cast<uint16_t>(b.y)), u3 = bf16_to_f32(static_cast<uint16_t>(b.y >> 16));
+            sww = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w, sww))));
+            swu = fmaf(a.x, u0, fmaf(a.y, u1, fmaf(a.z, u2, fmaf(a.w, u3, swu))));
+            suu = fmaf(u0, u0, fmaf(u1, u1, fmaf(u2, u2, fmaf(u3, u3, suu))));
+        }
+        ww += static_cast<double>(sww);
+        wu += static_cast<double>(swu);
+        uu += static_cast<double>(suu);
+    }
+    block_sum3(ww, wu, uu, sh);
+    if (threadIdx.x == 0) {
+        partials[3 * blockIdx.x + 0] = ww;
+        partials[3 * blockIdx.x + 1] = wu;
+        partials[3 * blockIdx.x + 2] = uu;
+    }
+}
+
+// w = R (w - a u) / |w - a u| with a = lr R / |u|, from the dot3 partials; in place.
+// |u| = 0 leaves the direction unchanged (a = 0); a zero W' leaves w unchanged.
+__global__ void __launch_bounds__(kMuonThreads) muonh_apply_kernel(float* __restrict__ w, int64_t ldw,
+                                                                   const uint16_t* __restrict__ u, int64_t ldu,
+                                                                   int64_t rows, int64_t cols,
+                                                                   const double* __restrict__ partials, int nparts,
+                                                                   float lr, float radius)
+{
+    __shared__ float coef[2];  // a, scale
+    if (threadIdx.x == 0) {
+        const double sww = sum_partials(partials, nparts, 0);
+        const double swu = sum_partials(partials, nparts, 1);
+        const double suu = sum_partials(partials, nparts, 2);
+        const double nu = sqrt(suu);
+        const double a = nu > 0.0 ? static_cast<double>(lr) * static_cast<double>(radius) / nu : 0.0;
+        double n2 = sww - 2.0 * a * swu + a * a * suu;
+        n2 = n2 > 0.0 ? n2 : 0.0;
+        coef[0] = static_cast<float>(a);
+        coef[1] = n2 > 0.0 ? static_cast<float>(static_cast<double>(radius) / sqrt(n2)) : 1.0f;
+    }
+    __syncthreads();
+    const float a = coef[0], scale = coef[1];
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        float4* wr = reinterpret_cast<float4*>(w + r * ldw);
+        const uint2* ur = reinterpret_cast<const uint2*>(u + r * ldu);
+        for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
+            float4 v = wr[j];
+            const uint2 b = ur[j];
+            v.x = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x)), v.x) * scale;
+            v.y = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x >> 16)), v.y) * scale;
+            v.z = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y)), v.z) * scale;
+            v.w = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y >> 16)), v.w) * scale;
+            wr[j] = v;
+        }
+    }
+}
+
+}  // namespace bfp8

@@ -139,6 +139,36 @@ int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, const float* s
                              const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
                              float* main_grad, int64_t ldmg, int64_t M, int64_t N, int64_t K, void* stream);
 
+/* MuonH update (Puro-2B article on en.roboind.com, section "From ordinary
+ * learning to effective learning": the update size is standardised on top of
+ * Muon and the weight is projected back to a fixed radius afterwards). Read
+ * plainly, with Frobenius norms |.|, U the Newton-Schulz orthogonalisation of
+ * the gradient G, learning rate lr and radius R:
+ *   X0 = G / (|G| + eps);  W' = W - lr R U / |U|;  W_new = R W' / |W'|.
+ * The Newton-Schulz iterations between the two calls are plain BF16 GEMMs
+ * (the Python binding runs them through cuBLAS). Sums are deterministic
+ * (fixed grid, fixed order). Matrices are row-major; cols a multiple of 4.
+ *   partials: caller-owned scratch of muonh_partials_len() doubles, 8-byte
+ *     aligned; overwritten by each call; calls that share it must be ordered.
+ * muonh_partials_len: writes the number of doubles; BFP8_EINVAL for NULL. */
+int muonh_partials_len(int* n);
+
+/* x[r][c] = bf16_rn(g[r][c] / (|g| + eps)).
+ *   g FP32 [rows][ldg] (16-byte aligned, ldg % 4 == 0), x BF16 [rows][ldx]
+ *   (8-byte aligned, ldx % 4 == 0), eps >= 0.
+ * Errors: BFP8_EINVAL (null, sizes, eps), BFP8_ESHAPE (cols % 4), BFP8_EALIGN. */
+int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, void* x, int64_t ldx,
+                    double* partials, float eps, void* stream);
+
+/* w = R (w - a u) / |w - a u| in place, a = lr R / |u| (a = 0 if |u| = 0; w is
+ * left unchanged if w - a u is zero). The norm of w - a u comes from
+ * |w|^2 - 2 a <w,u> + a^2 |u|^2, so w and u are read twice in all.
+ *   w FP32 [rows][ldw] (16-byte aligned, ldw % 4 == 0), u BF16 [rows][ldu]
+ *   (8-byte aligned, ldu % 4 == 0), lr >= 0, radius > 0.
+ * Errors: as muonh_normalize (lr, radius checked as BFP8_EINVAL). */
+int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                double* partials, float lr, float radius, void* stream);
+
 /* Human-readable name of a bfp8_status value (static string, never NULL). */
 const char* bfp8_status_string(int status);
 

@@ -25,7 +25,8 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
-                          "bfp8_set_gemm_cluster", "bfp8_set_gemm_promo_warps"}
+                          "bfp8_set_gemm_cluster", "bfp8_set_gemm_promo_warps",
+                          "muonh_partials_len", "muonh_normalize", "muonh_apply"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
         assert hasattr(cdll, n), n
@@ -105,3 +106,18 @@ def test_gemm_argument_checks(lib):
     assert acc(A, 256, A, 128, A, 256, A, 128, A, 100, 200, 128, 128, s) == EINVAL  # ldmg < K
     assert acc(A, 256, A, 128, A, 256, A, 128, A, 130, 200, 128, 128, s) == EALIGN  # ldmg % 4
     assert acc(A, 256, A, 128, A, 256, A, 128, A + 8, 128, 200, 128, 128, s) == EALIGN
+
+
+def test_muonh_argument_checks(lib):
+    s = None
+    f = ctypes.c_float
+    assert lib.muonh_partials_len(None) == EINVAL
+    assert lib.muonh_normalize(A, 4, 6, 8, A, 8, A, f(0.0), s) == ESHAPE       # cols % 4
+    assert lib.muonh_normalize(None, 4, 8, 8, A, 8, A, f(0.0), s) == EINVAL
+    assert lib.muonh_normalize(A, 4, 8, 4, A, 8, A, f(0.0), s) == EINVAL       # ldg < cols
+    assert lib.muonh_normalize(A + 4, 4, 8, 8, A, 8, A, f(0.0), s) == EALIGN
+    assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, f(-1.0), s) == EINVAL      # eps < 0
+    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, f(0.1), f(0.0), s) == EINVAL   # radius 0
+    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, f(-0.1), f(1.0), s) == EINVAL  # lr < 0
+    assert lib.muonh_apply(A, 10, A, 8, 4, 8, A, f(0.1), f(1.0), s) == EALIGN  # ldw % 4
+    assert lib.muonh_apply(A, 8, A + 2, 8, 4, 8, A, f(0.1), f(1.0), s) == EALIGN

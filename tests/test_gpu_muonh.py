@@ -1,0 +1,73 @@
+"""GPU parity of the MuonH update against the FP64 oracle (oracle/muonh.py).
+
+Bars:
+  * muonh_normalize: every BF16 output within one BF16 unit in the last place of
+    the exact quotient, 2^-7 |x_ref| (the FP32 product is rounded once more to BF16);
+  * muonh_apply (given U): FP32 element-wise arithmetic on FP64 sums,
+    |w - w_ref| <= 4e-6 |w_ref| + 4e-6 rms(w_ref), and |w|_F = R within 1e-5;
+  * full update: the Newton-Schulz GEMMs run in BF16 (FP32 accumulation), which
+    moves U by about 1 % of its norm against FP64 on random matrices; the bar is
+    |W - W_ref|_F <= 5 % of the step, i.e. 0.05 lr R.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import muonh as ref
+
+import blockwise_fp8_linear_weight_b300 as bfp8
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(shape, seed, scale=1.0):
+    return (np.random.default_rng(seed).standard_normal(shape) * scale).astype(np.float32)
+
+
+@pytest.mark.parametrize("shape", [(4, 4), (256, 512), (300, 1028), (2048, 6144)])
+def test_normalize_parity(shape):
+    G = _rand(shape, 1)
+    x = bfp8.muonh_normalize(torch.from_numpy(G).cuda())
+    torch.cuda.synchronize()
+    got = x.float().cpu().numpy().astype(np.float64)
+    want = ref.normalize(G)
+    assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-30)
+
+
+@pytest.mark.parametrize("shape", [(8, 16), (512, 256), (2048, 6144)])
+def test_apply_parity_and_radius(shape):
+    W = _rand(shape, 2, 0.02)
+    U = torch.from_numpy(_rand(shape, 3)).to(torch.bfloat16)
+    R, lr = 1.7, 0.05
+    w = torch.from_numpy(W.copy()).cuda()
+    bfp8.muonh_apply(w, U.cuda(), lr, R)
+    torch.cuda.synchronize()
+    got = w.cpu().numpy().astype(np.float64)
+    want = ref.apply(W, U.float().numpy(), lr, R)
+    rms = np.sqrt(np.mean(want ** 2))
+    assert np.all(np.abs(got - want) <= 4e-6 * np.abs(want) + 4e-6 * rms)
+    assert abs(np.linalg.norm(got) - R) <= 1e-5 * R
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (512, 256), (2048, 6144)])
+def test_full_update_against_fp64_oracle(shape):
+    W = _rand(shape, 4, 0.02)
+    G = _rand(shape, 5)
+    R, lr = float(np.linalg.norm(W.astype(np.float64))), 0.02
+    w = torch.from_numpy(W.copy()).cuda()
+    bfp8.muonh_update(w, torch.from_numpy(G).cuda(), lr, R)
+    torch.cuda.synchronize()
+    got = w.cpu().numpy().astype(np.float64)
+    want = ref.update(W, G, lr, R)
+    assert np.linalg.norm(got - want) <= 0.05 * lr * R
+    assert abs(np.linalg.norm(got) - R) <= 1e-5 * R
+
+
+def test_update_is_deterministic():
+    W = torch.from_numpy(_rand((1024, 2048), 6, 0.02)).cuda()
+    G = torch.from_numpy(_rand((1024, 2048), 7)).cuda()
+    w1, w2 = W.clone(), W.clone()
+    bfp8.muonh_update(w1, G, 0.02, 1.0)
+    bfp8.muonh_update(w2, G, 0.02, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(w1, w2)
