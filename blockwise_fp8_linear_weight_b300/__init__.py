@@ -72,8 +72,8 @@ def load_library(path: str = LIB_PATH):
         "bfp8_set_gemm_cluster": [c_int],
         "bfp8_set_gemm_promo_warps": [c_int],
         "muonh_partials_len": [ctypes.POINTER(c_int)],
-        "muonh_normalize": [p, i64, i64, i64, p, i64, p, ctypes.c_float, p],
-        "muonh_apply": [p, i64, p, i64, i64, i64, p, ctypes.c_float, ctypes.c_float, p],
+        "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
+        "muonh_apply": [p, i64, p, i64, i64, i64, p, i64, ctypes.c_float, ctypes.c_float, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -365,8 +365,9 @@ def muonh_normalize(g, x=None, eps: float = 1e-7, partials=None):
     rows, cols = g.shape
     x = torch.empty((rows, cols), dtype=torch.bfloat16, device=g.device) if x is None else x
     partials = _muonh_partials(g.device) if partials is None else partials
+    _req(partials, torch.float64, "partials", ndim=1)
     _check("muonh_normalize", lib.muonh_normalize(_ptr(g), rows, cols, g.stride(0), _ptr(x), x.stride(0),
-                                                  _ptr(partials), float(eps), _stream()))
+                                                  _ptr(partials), partials.numel(), float(eps), _stream()))
     return x
 
 
@@ -379,8 +380,9 @@ def muonh_apply(w, u, lr: float, radius: float, partials=None):
         raise ValueError("u must have w's shape")
     rows, cols = w.shape
     partials = _muonh_partials(w.device) if partials is None else partials
+    _req(partials, torch.float64, "partials", ndim=1)
     _check("muonh_apply", lib.muonh_apply(_ptr(w), w.stride(0), _ptr(u), u.stride(0), rows, cols,
-                                          _ptr(partials), float(lr), float(radius), _stream()))
+                                          _ptr(partials), partials.numel(), float(lr), float(radius), _stream()))
     return w
 
 

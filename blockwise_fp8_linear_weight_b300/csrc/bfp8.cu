@@ -605,7 +605,7 @@ extern "C" int muonh_partials_len(int* n)
 }
 
 extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, void* x, int64_t ldx,
-                               double* partials, float eps, void* stream)
+                               double* partials, int64_t partials_len, float eps, void* stream)
 {
     if (rows < 1 || cols < 1)
         return BFP8_EINVAL;
@@ -620,6 +620,8 @@ extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64
     if (rc != BFP8_OK)
         return rc;
     const int grid = muonh_grid(dev);
+    if (partials_len < 3 * static_cast<int64_t>(grid))
+        return BFP8_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     muonh_sumsq_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials);
     muonh_scale_bf16_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials, grid, eps,
@@ -628,7 +630,7 @@ extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64
 }
 
 extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
-                           double* partials, float lr, float radius, void* stream)
+                           double* partials, int64_t partials_len, float lr, float radius, void* stream)
 {
     if (rows < 1 || cols < 1)
         return BFP8_EINVAL;
@@ -643,6 +645,8 @@ extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, in
     if (rc != BFP8_OK)
         return rc;
     const int grid = muonh_grid(dev);
+    if (partials_len < 3 * static_cast<int64_t>(grid))
+        return BFP8_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* ub = static_cast<const uint16_t*>(u);
     muonh_dot3_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials);

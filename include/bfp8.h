@@ -148,8 +148,9 @@ int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, const float* s
  * The Newton-Schulz iterations between the two calls are plain BF16 GEMMs
  * (the Python binding runs them through cuBLAS). Sums are deterministic
  * (fixed grid, fixed order). Matrices are row-major; cols a multiple of 4.
- *   partials: caller-owned scratch of muonh_partials_len() doubles, 8-byte
- *     aligned; overwritten by each call; calls that share it must be ordered.
+ *   partials, partials_len: caller-owned scratch of at least
+ *     muonh_partials_len() doubles, 8-byte aligned (BFP8_EINVAL if shorter);
+ *     overwritten by each call; calls that share it must be ordered.
  * muonh_partials_len: writes the number of doubles; BFP8_EINVAL for NULL. */
 int muonh_partials_len(int* n);
 
@@ -158,7 +159,7 @@ int muonh_partials_len(int* n);
  *   (8-byte aligned, ldx % 4 == 0), eps >= 0.
  * Errors: BFP8_EINVAL (null, sizes, eps), BFP8_ESHAPE (cols % 4), BFP8_EALIGN. */
 int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, void* x, int64_t ldx,
-                    double* partials, float eps, void* stream);
+                    double* partials, int64_t partials_len, float eps, void* stream);
 
 /* w = R (w - a u) / |w - a u| in place, a = lr R / |u| (a = 0 if |u| = 0; w is
  * left unchanged if w - a u is zero). The norm of w - a u comes from
@@ -167,7 +168,7 @@ int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, voi
  *   (8-byte aligned, ldu % 4 == 0), lr >= 0, radius > 0.
  * Errors: as muonh_normalize (lr, radius checked as BFP8_EINVAL). */
 int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
-                double* partials, float lr, float radius, void* stream);
+                double* partials, int64_t partials_len, float lr, float radius, void* stream);
 
 /* Human-readable name of a bfp8_status value (static string, never NULL). */
 const char* bfp8_status_string(int status);

@@ -112,12 +112,15 @@ def test_muonh_argument_checks(lib):
     s = None
     f = ctypes.c_float
     assert lib.muonh_partials_len(None) == EINVAL
-    assert lib.muonh_normalize(A, 4, 6, 8, A, 8, A, f(0.0), s) == ESHAPE       # cols % 4
-    assert lib.muonh_normalize(None, 4, 8, 8, A, 8, A, f(0.0), s) == EINVAL
-    assert lib.muonh_normalize(A, 4, 8, 4, A, 8, A, f(0.0), s) == EINVAL       # ldg < cols
-    assert lib.muonh_normalize(A + 4, 4, 8, 8, A, 8, A, f(0.0), s) == EALIGN
-    assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, f(-1.0), s) == EINVAL      # eps < 0
-    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, f(0.1), f(0.0), s) == EINVAL   # radius 0
-    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, f(-0.1), f(1.0), s) == EINVAL  # lr < 0
-    assert lib.muonh_apply(A, 10, A, 8, 4, 8, A, f(0.1), f(1.0), s) == EALIGN  # ldw % 4
-    assert lib.muonh_apply(A, 8, A + 2, 8, 4, 8, A, f(0.1), f(1.0), s) == EALIGN
+    assert lib.muonh_normalize(A, 4, 6, 8, A, 8, A, 1 << 12, f(0.0), s) == ESHAPE       # cols % 4
+    assert lib.muonh_normalize(None, 4, 8, 8, A, 8, A, 1 << 12, f(0.0), s) == EINVAL
+    assert lib.muonh_normalize(A, 4, 8, 4, A, 8, A, 1 << 12, f(0.0), s) == EINVAL       # ldg < cols
+    assert lib.muonh_normalize(A + 4, 4, 8, 8, A, 8, A, 1 << 12, f(0.0), s) == EALIGN
+    assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, 1 << 12, f(-1.0), s) == EINVAL      # eps < 0
+    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, 1 << 12, f(0.1), f(0.0), s) == EINVAL   # radius 0
+    assert lib.muonh_apply(A, 8, A, 8, 4, 8, A, 1 << 12, f(-0.1), f(1.0), s) == EINVAL  # lr < 0
+    assert lib.muonh_apply(A, 10, A, 8, 4, 8, A, 1 << 12, f(0.1), f(1.0), s) == EALIGN  # ldw % 4
+    assert lib.muonh_apply(A, 8, A + 2, 8, 4, 8, A, 1 << 12, f(0.1), f(1.0), s) == EALIGN
+    # a partials buffer shorter than muonh_partials_len() is refused (without a B300 the
+    # device query refuses first)
+    assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, 0, f(0.0), s) != OK

@@ -71,3 +71,11 @@ def test_update_is_deterministic():
     bfp8.muonh_update(w2, G, 0.02, 1.0)
     torch.cuda.synchronize()
     assert torch.equal(w1, w2)
+
+
+def test_short_partials_buffer_is_refused():
+    g = torch.zeros((8, 16), dtype=torch.float32, device="cuda")
+    short = torch.zeros(3, dtype=torch.float64, device="cuda")
+    with pytest.raises(bfp8.Bfp8Error) as e:
+        bfp8.muonh_normalize(g, partials=short)
+    assert e.value.code == -1
