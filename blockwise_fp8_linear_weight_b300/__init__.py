@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH):
         "muonh_partials_len": [ctypes.POINTER(c_int)],
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
         "muonh_apply": [p, i64, p, i64, i64, i64, p, i64, ctypes.c_float, ctypes.c_float, p],
+        "muonh_apply_static": [p, i64, p, i64, i64, i64, ctypes.c_float, ctypes.c_float, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -383,6 +384,19 @@ def muonh_apply(w, u, lr: float, radius: float, partials=None):
     _req(partials, torch.float64, "partials", ndim=1)
     _check("muonh_apply", lib.muonh_apply(_ptr(w), w.stride(0), _ptr(u), u.stride(0), rows, cols,
                                           _ptr(partials), partials.numel(), float(lr), float(radius), _stream()))
+    return w
+
+
+def muonh_apply_static(w, u, lr: float, radius: float):
+    """muonh_apply with the library's own device scratch (calls on a device must be ordered)."""
+    lib = load_library()
+    _req(w, torch.float32, "w")
+    _req(u, torch.bfloat16, "u")
+    if u.shape != w.shape:
+        raise ValueError("u must have w's shape")
+    rows, cols = w.shape
+    _check("muonh_apply_static", lib.muonh_apply_static(_ptr(w), w.stride(0), _ptr(u), u.stride(0), rows, cols,
+                                                        float(lr), float(radius), _stream()))
     return w
 
 

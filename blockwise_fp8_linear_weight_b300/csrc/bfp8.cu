@@ -589,6 +589,10 @@ int muonh_grid(int dev)
 {
     return 2 * sm_count(dev);
 }
+
+// Device-wide partial sums for muonh_apply_static (room for grids of up to 512 CTAs).
+constexpr int64_t kStaticPartials = 3 * 512;
+__device__ __align__(256) double g_muonh_partials[kStaticPartials];
 }  // namespace
 }  // namespace bfp8
 
@@ -629,14 +633,16 @@ extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64
     return launch_status();
 }
 
-extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
-                           double* partials, int64_t partials_len, float lr, float radius, void* stream)
+static int muonh_apply_impl(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                            double* partials, int64_t partials_len, bool static_partials, float lr, float radius,
+                            void* stream)
 {
     if (rows < 1 || cols < 1)
         return BFP8_EINVAL;
     if (cols % 4 || rows > kMaxDim || cols > kMaxDim)
         return BFP8_ESHAPE;
-    if (!w || !u || !partials || ldw < cols || ldu < cols || !(lr >= 0.0f) || !(radius > 0.0f))
+    if (!w || !u || (!static_partials && !partials) || ldw < cols || ldu < cols || !(lr >= 0.0f) ||
+        !(radius > 0.0f))
         return BFP8_EINVAL;
     if (!aligned(w, 16) || ldw % 4 || !aligned(u, 8) || ldu % 4 || !aligned(partials, 8))
         return BFP8_EALIGN;
@@ -644,6 +650,13 @@ extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, in
     int rc = check_arch(&dev);
     if (rc != BFP8_OK)
         return rc;
+    if (static_partials) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_muonh_partials) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        partials = static_cast<double*>(p);
+        partials_len = kStaticPartials;
+    }
     const int grid = muonh_grid(dev);
     if (partials_len < 3 * static_cast<int64_t>(grid))
         return BFP8_EINVAL;
@@ -652,6 +665,18 @@ extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, in
     muonh_dot3_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials);
     muonh_apply_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
     return launch_status();
+}
+
+extern "C" int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                           double* partials, int64_t partials_len, float lr, float radius, void* stream)
+{
+    return muonh_apply_impl(w, ldw, u, ldu, rows, cols, partials, partials_len, false, lr, radius, stream);
+}
+
+extern "C" int muonh_apply_static(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                                  float lr, float radius, void* stream)
+{
+    return muonh_apply_impl(w, ldw, u, ldu, rows, cols, nullptr, 0, true, lr, radius, stream);
 }
 
 // =================================================================== misc

@@ -170,6 +170,14 @@ int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, voi
 int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
                 double* partials, int64_t partials_len, float lr, float radius, void* stream);
 
+/* muonh_apply without caller scratch: the partial sums live in one
+ * library-owned device array per device (grids of up to 512 CTAs; BFP8_EINVAL
+ * on a device that would need more). Calls on a device share that array, so
+ * they must be ordered (one stream, or synchronised); results are bit-identical
+ * to muonh_apply. Arguments and errors otherwise as muonh_apply. */
+int muonh_apply_static(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
+                       float lr, float radius, void* stream);
+
 /* Human-readable name of a bfp8_status value (static string, never NULL). */
 const char* bfp8_status_string(int status);
 

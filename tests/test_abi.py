@@ -26,7 +26,7 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
                           "bfp8_set_gemm_cluster", "bfp8_set_gemm_promo_warps",
-                          "muonh_partials_len", "muonh_normalize", "muonh_apply"}
+                          "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
         assert hasattr(cdll, n), n
@@ -124,3 +124,5 @@ def test_muonh_argument_checks(lib):
     # a partials buffer shorter than muonh_partials_len() is refused (without a B300 the
     # device query refuses first)
     assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, 0, f(0.0), s) != OK
+    assert lib.muonh_apply_static(A, 8, A, 8, 4, 8, f(0.1), f(0.0), s) == EINVAL   # radius 0
+    assert lib.muonh_apply_static(A, 8, A, 8, 4, 6, f(0.1), f(1.0), s) == ESHAPE   # cols % 4

@@ -79,3 +79,20 @@ def test_short_partials_buffer_is_refused():
     with pytest.raises(bfp8.Bfp8Error) as e:
         bfp8.muonh_normalize(g, partials=short)
     assert e.value.code == -1
+
+
+@pytest.mark.parametrize("shape", [(8, 16), (2048, 6144)])
+def test_apply_static_scratch_matches_caller_scratch(shape):
+    W = _rand(shape, 12, 0.02)
+    U = torch.from_numpy(_rand(shape, 13)).to(torch.bfloat16).cuda()
+    R, lr = 2.0, 0.03
+    w1 = torch.from_numpy(W.copy()).cuda()
+    w2 = w1.clone()
+    bfp8.muonh_apply(w1, U, lr, R)
+    bfp8.muonh_apply_static(w2, U, lr, R)
+    torch.cuda.synchronize()
+    assert torch.equal(w1, w2)
+    want = ref.apply(W, U.float().cpu().numpy(), lr, R)
+    got = w2.cpu().numpy().astype(np.float64)
+    rms = np.sqrt(np.mean(want ** 2))
+    assert np.all(np.abs(got - want) <= 4e-6 * np.abs(want) + 4e-6 * rms)
