@@ -87,43 +87,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// As mbar_wait, but polls with the non-suspending test_wait: the thread sees
-// the phase complete within a few cycles instead of whenever a suspended
-// try_wait is resumed. Meant for a single latency-critical thread.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                               unsigned* status)
-{
-    if (mbar_test_wait(bar, parity))
-        return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test_wait(bar, parity))
-            return true;
-        if ((it & 63u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(status, kDevTimeout);
-                return false;
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
 {
@@ -201,27 +164,6 @@ __device__ __forceinline__ void tma_store_wait_read_all()
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Barrier over `nthreads` threads that also ORs a predicate across them: every
-// participant gets the same answer.
-__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
-        : "memory");
-    return r != 0;
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -312,22 +254,6 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta
         : "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i), columns col..col+31.
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-
 // 32 lanes x 64 consecutive 32-bit columns starting at taddr, waited for, and
 // returned as 32 packed pairs of neighbouring columns (column 2i in the low
 // word of p[i]). Loading, waiting and pairing in one block lets the register
@@ -396,11 +322,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t s)
     return d;
 }
 
-__device__ __forceinline__ void tmem_ld_wait()
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ packed FP32 arithmetic
 // Two FP32 values travel as one 64-bit register pair (low word = first value)
 // and are processed by one instruction; each lane is rounded to nearest-even
@@ -410,16 +331,6 @@ __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi)
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
-}
-
-// acc = {lo, hi} * s + acc  (lo, hi: raw FP32 bits, e.g. from tcgen05.ld)
-__device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint32_t lo, uint32_t hi, uint64_t s)
-{
-    asm("{\n\t.reg .b64 p;\n\t"
-        "mov.b64 p, {%1, %2};\n\t"
-        "fma.rn.f32x2 %0, p, %3, %0;\n\t}"
-        : "+l"(acc)
-        : "r"(lo), "r"(hi), "l"(s));
 }
 
 // {lo, hi} * s
@@ -478,15 +389,6 @@ __device__ __forceinline__ float bf16_lo(uint32_t w)
 __device__ __forceinline__ float bf16_hi(uint32_t w)
 {
     return __uint_as_float(w & 0xFFFF0000u);
-}
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
 }
 
 }  // namespace bfp8
