@@ -325,6 +325,103 @@ struct QuantArgs {
     unsigned* status;
 };
 
+// Row pass over 8 row tiles per half-warp (1x128 tiles along the columns):
+// codes to q [R][C], scales to s [C/128][R].
+__device__ __forceinline__ void row_tiles8(const uint32_t (*tile)[64], const ScaleTables& stab, const QuantArgs& a,
+                                           int64_t rb, int64_t cb, int r_local, int rstep)
+{
+    const int tid = threadIdx.x;
+    const int sub = tid & 15;
+    // The thread covers rows r_local + rstep j (j = 0..7) of the block, columns
+    // 8 (t%16) .. +7; a half-warp owns one row tile per j. The half-warp
+    // reduces its 8 tiles at once with a butterfly that halves the number of
+    // tiles each lane carries per step (lane bit 3 picks 4 of the 8, bit 2 two
+    // of those, bit 1 one), so that lanes 2j and 2j+1 end with tile j's amax;
+    // each lane computes that tile's scale, and the encoding pass fetches a
+    // tile's scale by shuffle.
+    uint32_t m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        m[j] = absmax_pairs(*reinterpret_cast<const uint4*>(&tile[r_local + rstep * j][sub * 4]));
+    {
+        const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t send = b3 ? m[i] : m[i + 4], keep = b3 ? m[i + 4] : m[i];
+            m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t send = b2 ? m[i] : m[i + 2], keep = b2 ? m[i + 2] : m[i];
+            m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+        }
+        const uint32_t send = b1 ? m[0] : m[1], keep = b1 ? m[1] : m[0];
+        m[0] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+        m[0] = bf16x2_max(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
+    }
+    const TileScale mine = tile_scale_tab(fmaxf(bf16_lo(m[0]), bf16_hi(m[0])), stab);  // tile sub >> 1
+    const int lane = tid & 31;
+    const int64_t r0 = rb * 128 + r_local;  // the thread's row for j = 0
+    // lanes 2j store tile j's scale (row r0 + rstep j of their half-warp)
+    if ((sub & 1) == 0 && r0 + rstep * (sub >> 1) < a.R)
+        a.s[cb * a.lds + r0 + rstep * (sub >> 1)] = mine.s;
+    const float bc_sp = mine.pre != 1.0f ? mine.sp : -mine.sp;  // sign carries the pre-scaling flag
+    const int rows_left = static_cast<int>(a.R - r0 > 128 ? 128 : a.R - r0);
+    uint8_t* qrow = a.q + r0 * a.ldq + cb * 128 + sub * 8;
+    const int64_t qstep = rstep * a.ldq;
+#pragma unroll 2
+    for (int j = 0; j < 8; ++j) {
+        const int src = (lane & 16) | (2 * j);
+        const PairScale ps = pair_scale_bcast(__shfl_sync(0xffffffffu, mine.y, src),
+                                              __shfl_sync(0xffffffffu, bc_sp, src));
+        if (rstep * j < rows_left) {
+            const uint4 v = *reinterpret_cast<const uint4*>(&tile[r_local + rstep * j][sub * 4]);
+            *reinterpret_cast<uint2*>(qrow) = codes8(v, ps);
+        }
+        qrow += qstep;
+    }
+}
+
+// Column pass by warps 4-7 only (while warps 0-3 do the row pass): thread
+// t' = t - 128 takes the column pair 32 ((t'/32) % 2) + lane over rows
+// 64 (t'/64) .. +63; the two row halves combine their amax through shared
+// memory behind a barrier of these 128 threads only.
+__device__ __forceinline__ void column_pass_4w(const uint32_t (*tile)[64], uint32_t (*part)[64], const ScaleTables& tab,
+                                               int64_t cb, int64_t rb, uint8_t* __restrict__ qt, int64_t ldqt,
+                                               float* __restrict__ st, int64_t ldst)
+{
+    const int t = threadIdx.x - 128;
+    const int w = t >> 5, lane = t & 31;
+    const int half = w >> 1;
+    const int cw = (w & 1) * 32 + lane;
+    const int col = 2 * cw;
+    uint32_t m = 0;
+#pragma unroll 16
+    for (int i = 0; i < 64; ++i)
+        m = bf16x2_maxabs(m, tile[half * 64 + i][cw]);
+    part[half][cw] = m & 0x7FFF7FFFu;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    m = bf16x2_max(part[0][cw], part[1][cw]);
+    const TileScale s0 = tile_scale_tab(bf16_lo(m), tab), s1 = tile_scale_tab(bf16_hi(m), tab);
+    const PairScale ps = pair_scale(s0, s1);
+    uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + half * 64;
+    uint8_t* out1 = out0 + ldqt;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {  // rows half*64 + 32 q .. +31
+        uint32_t c0[8], c1[8];
+        if (ps.scaled)
+            column_encode<true>(tile, 2 * half + q, cw, ps, c0, c1);
+        else
+            column_encode<false>(tile, 2 * half + q, cw, ps, c0, c1);
+        reinterpret_cast<uint4*>(out0 + 32 * q)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+        reinterpret_cast<uint4*>(out0 + 32 * q)[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
+        reinterpret_cast<uint4*>(out1 + 32 * q)[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+        reinterpret_cast<uint4*>(out1 + 32 * q)[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+    }
+    if (half == 0)
+        *reinterpret_cast<float2*>(st + rb * ldst + cb * 128 + col) = make_float2(s0.s, s1.s);
+}
+
 constexpr int kQuantTileBytes = 128 * 128 * 2;
 constexpr int kQuantSmemBytes = 2 * kQuantTileBytes + 1024;  // two tiles + alignment slack
 
@@ -378,58 +475,21 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
             break;
         const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + (i & 1) * kQuantTileBytes);
 
-        if (MODE == MODE_ROWS || MODE == MODE_DUAL) {
-            // thread t: rows t/16 + 16 j, columns 8 (t%16) .. +7; a half-warp owns one
-            // row tile per j (j = 0..7). The half-warp reduces its 8 tiles at once
-            // with a butterfly that halves the number of tiles each lane carries
-            // per step (lane bit 3 picks 4 of the 8, bit 2 two of those, bit 1
-            // one), so that lanes 2j and 2j+1 end with tile j's amax; each lane
-            // computes that tile's scale, and the encoding pass fetches a tile's
-            // scale by shuffle.
-            uint32_t m[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                m[j] = absmax_pairs(*reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4]));
-            {
-                const bool b3 = sub & 8, b2 = sub & 4, b1 = sub & 2;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t send = b3 ? m[i] : m[i + 4], keep = b3 ? m[i + 4] : m[i];
-                    m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-                }
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const uint32_t send = b2 ? m[i] : m[i + 2], keep = b2 ? m[i + 2] : m[i];
-                    m[i] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-                }
-                const uint32_t send = b1 ? m[0] : m[1], keep = b1 ? m[1] : m[0];
-                m[0] = bf16x2_max(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-                m[0] = bf16x2_max(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));
-            }
-            const TileScale mine = tile_scale_tab(fmaxf(bf16_lo(m[0]), bf16_hi(m[0])), stab);  // tile sub >> 1
-            const int lane = tid & 31;
-            const int64_t r0 = rb * 128 + (tid >> 4);  // the thread's row for j = 0
-            // lanes 2j store tile j's scale (rows r0 - ... + 16 j of their half-warp)
-            if ((sub & 1) == 0 && r0 + 16 * (sub >> 1) < a.R)
-                a.s[cb * a.lds + r0 + 16 * (sub >> 1)] = mine.s;
-            const float bc_sp = mine.pre != 1.0f ? mine.sp : -mine.sp;  // sign carries the pre-scaling flag
-            const int rows_left = static_cast<int>(a.R - r0 > 128 ? 128 : a.R - r0);
-            uint8_t* qrow = a.q + r0 * a.ldq + cb * 128 + sub * 8;
-            const int64_t qstep = 16 * a.ldq;
-#pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                const int src = (lane & 16) | (2 * j);
-                const PairScale ps = pair_scale_bcast(__shfl_sync(0xffffffffu, mine.y, src),
-                                                      __shfl_sync(0xffffffffu, bc_sp, src));
-                if (16 * j < rows_left) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4]);
-                    *reinterpret_cast<uint2*>(qrow) = codes8(v, ps);
-                }
-                qrow += qstep;
+        if (MODE == MODE_ROWS) {
+            row_tiles8(tile, stab, a, rb, cb, tid >> 4, 16);
+        }
+        if (MODE == MODE_COLS)
+            column_pass(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+        if (MODE == MODE_DUAL) {
+            // warps 0-3: row tiles (two groups of 8 per half-warp); warps 4-7, at the
+            // same time: transposed tiles; the two only share the block
+            if (tid < 128) {
+                row_tiles8(tile, stab, a, rb, cb, tid >> 4, 8);
+                row_tiles8(tile, stab, a, rb, cb, (tid >> 4) + 64, 8);
+            } else {
+                column_pass_4w(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
             }
         }
-        if (MODE == MODE_COLS || MODE == MODE_DUAL)
-            column_pass(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
         if (MODE == MODE_WEIGHT) {
             uint32_t m = 0;
 #pragma unroll
