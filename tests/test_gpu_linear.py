@@ -95,3 +95,40 @@ def test_main_gradient_mode_accumulates_micro_batches():
     assert torch.allclose(layer.main_grad, 2.0 * once, rtol=2.0 ** -23, atol=0.0)
     layer.zero_main_grad()
     assert torch.count_nonzero(layer.main_grad) == 0
+
+
+def test_training_step_replays_from_a_cuda_graph():
+    """The six calls of a step can be captured in a CUDA graph (after one eager step sets the
+    library's lazily initialised state) and replayed: the replay gives the eager step's bits,
+    and a replay after new inputs are copied into the captured buffers gives their results."""
+    lin, x, w, dy = _case(M=640, K=512, N=768)
+    xd, wd, dyd = to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy)
+    layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N)
+    layer.forward(xd, wd)
+    layer.backward(dyd)
+    torch.cuda.synchronize()
+    want = [t.clone() for t in (layer.y, layer.dx, layer.dw)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(xd, wd)
+        layer.backward(dyd)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(xd, wd)
+        layer.backward(dyd)
+    for t in (layer.y, layer.dx, layer.dw):
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for got, ref in zip((layer.y, layer.dx, layer.dw), want):
+        assert torch.equal(got, ref)
+    # new inputs in the captured buffers: the replay computes them (2x on x scales y and dW by 2)
+    xd.mul_(2.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y, 2.0 * want[0])
+    assert torch.equal(layer.dw, 2.0 * want[2])
+    assert torch.equal(layer.dx, want[1])
