@@ -629,13 +629,19 @@ def quant_bytes(R: int, C: int) -> int:
     return 2 * R * C + R * C + 4 * R * (C // 128)
 
 
-def _kernel_sha():
-    """Hash of the kernel sources: a stored ncu traffic figure is only used while it still matches."""
+def _kernel_sha(csrc=None):
+    """Hash of the kernel sources with comments and blank space removed: a stored ncu traffic
+    figure is only used while the code it was captured on is unchanged."""
     import hashlib
+    import re
+    csrc = csrc or os.path.join(ROOT, "blockwise_fp8_linear_weight_b300", "csrc")
     h = hashlib.sha256()
     for f in ("gemm.cuh", "ptx.cuh", "quant.cuh", "bfp8.cu"):
-        with open(os.path.join(ROOT, "blockwise_fp8_linear_weight_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

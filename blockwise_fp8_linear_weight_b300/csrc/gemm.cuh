@@ -29,9 +29,10 @@
 //               per chunk into one of two TMEM accumulators of BN columns;
 //   warp 2      producer of the scale ring (TMA for the per-row and per-column
 //               scales; plain loads for the scalar B scales);
-//   warps 4..11 promotion: warp w owns TMEM lanes 32 (w%4) .. +31 (output rows)
-//               and BN/2 columns; per chunk it reads the partial sums with
-//               tcgen05.ld (two loads in flight per wait), releases the TMEM
+//   warps 4..   promotion (8 warps by default; 12 or 16 as options): warp w
+//               owns TMEM lanes 32 (w%4) .. +31 (output rows) and BN/(PW/4)
+//               columns; per chunk it reads the partial sums with tcgen05.ld
+//               (64 columns per load and wait), releases the TMEM
 //               buffer and accumulates  acc += partial * (sA * sB)  in FP32
 //               registers with packed two-lane FP32 instructions (scalar FP32
 //               instructions issued at this rate halve the tensor core's MMA
@@ -45,7 +46,8 @@
 // With BN = 256 the promotion warps need more than the 168 registers a
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
 // warpgroup to the promotion warpgroups (56/224, or 64/216 with per-column
-// B scales), within the launch budget of 384 x 168.
+// B scales), within the launch budget of 384 x 168 (12 promotion warps at
+// BN = 192: 56/152 within 512 x 128; 16 warps: 32/112 within 640 x 96).
 // Every mbarrier wait is bounded (mbar_wait); a timeout sets the library's
 // device status word and the kernel unwinds without hanging.
 #pragma once
