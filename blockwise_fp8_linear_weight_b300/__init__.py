@@ -69,7 +69,6 @@ def load_library(path: str = LIB_PATH):
         "fp8_block_gemm_wgrad_acc": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
         "bfp8_last_device_status": [p],
         "bfp8_set_gemm_tile_n": [c_int],
-        "bfp8_set_gemm_cluster": [c_int],
         "bfp8_set_gemm_promo_warps": [c_int],
         "muonh_partials_len": [ctypes.POINTER(c_int)],
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
@@ -245,14 +244,6 @@ def set_gemm_tile_n(tile_n: int) -> int:
     rc = load_library().bfp8_set_gemm_tile_n(int(tile_n))
     if rc < 0:
         raise ValueError("tile_n must be 0, 128, 192 or 256")
-    return rc
-
-
-def set_gemm_cluster(cluster: int) -> int:
-    """CTAs per cluster for 256-wide GEMM tiles: 0 (automatic), 1 or 2. Returns the previous value."""
-    rc = load_library().bfp8_set_gemm_cluster(int(cluster))
-    if rc < 0:
-        raise ValueError("cluster must be 0, 1 or 2")
     return rc
 
 

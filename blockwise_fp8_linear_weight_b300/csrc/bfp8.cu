@@ -28,7 +28,6 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;  // TMA coordinates are in
 constexpr int64_t kMaxGridY = 65535;
 
 std::atomic<int> g_tile_n{0};
-std::atomic<int> g_cluster{0};
 std::atomic<int> g_promo_warps{8};
 
 // ----------------------------------------------------------------- helpers
@@ -142,37 +141,6 @@ struct GemmProblem {
     int64_t gm, gn, gk;
 };
 
-// Clusters of this kernel that fit on the device at once (one CTA per SM), cached.
-template <class Cfg>
-int max_clusters(int dev)
-{
-    static std::atomic<int> cache[kMaxDevices];
-    int n = cache[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        n = sm_count(dev) / Cfg::CLUSTER;
-        if (Cfg::CLUSTER > 1) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(n * Cfg::CLUSTER));
-            cfg.blockDim = dim3(Cfg::THREADS);
-            cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = Cfg::CLUSTER;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int active = 0;
-            if (cudaOccupancyMaxActiveClusters(&active, bfp8_gemm_kernel<Cfg>, &cfg) == cudaSuccess && active > 0)
-                n = std::min(n, active);
-        }
-        if (n < 1)
-            n = 1;
-        cache[dev].store(n, std::memory_order_relaxed);
-    }
-    return n;
-}
-
 template <class Cfg>
 int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int dev)
 {
@@ -184,7 +152,7 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
         ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gn, p.gk, p.ldb, 128, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     else
-        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN / Cfg::CLUSTER,
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN,
                             CU_TENSOR_MAP_SWIZZLE_128B);
     // scales: one box holds SGROUP chunks (rows) of 128 (A) or BN (B) scales
     ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, Cfg::SGROUP,
@@ -228,29 +196,14 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     // sweep along N first when B is the smaller operand (it then stays in L2
     // while the larger A is streamed once), along M otherwise
     args.n_fastest = p.gn < p.gm ? 1 : 0;
-    args.d = static_cast<uint16_t*>(p.d);
-    args.ldd = p.ldd;
     args.sb_scalar = p.sb;
     args.sb_col_stride = p.sb_col_stride;
     args.sb_chunk_stride = p.sb_chunk_stride;
     args.status = status;
-    const int64_t super_tiles =
-        static_cast<int64_t>((args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER) * args.tiles_n;
-    const int clusters = static_cast<int>(std::min<int64_t>(super_tiles, max_clusters<Cfg>(dev)));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * Cfg::CLUSTER));
-    cfg.blockDim = dim3(Cfg::THREADS);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = Cfg::CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmSA, tmSB, tmD, args) != cudaSuccess)
-        return BFP8_ELAUNCH;
+    // persistent grid: one CTA per SM, or one per tile if there are fewer tiles
+    const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
+    const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
+    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
     return launch_status();
 }
 
@@ -264,8 +217,8 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
     unsigned* status = device_status_ptr(dev);
     if (!status)
         return BFP8_ELAUNCH;
-    if (EPI == EPI_F32_ADD)  // one configuration: 256-wide tiles, one CTA per cluster, 8 promotion warps
-        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1, EPI_F32_ADD>>(p, status, stream, dev);
+    if (EPI == EPI_F32_ADD)  // one configuration: 256-wide tiles, 8 promotion warps
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, EPI_F32_ADD>>(p, status, stream, dev);
     int tn = g_tile_n.load(std::memory_order_relaxed);
     if (tn == 0)
         tn = 256;
@@ -274,16 +227,11 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
     if constexpr (!B_MN) {
         // 192-wide tiles: 12 promotion warps of 64 columns (one TMEM load per chunk each)
         if (tn == 192)
-            return run_gemm<GemmConfig<192, 4, B_MN, SB_VEC, 1, EPI_BF16_TMA, 12>>(p, status, stream, dev);
+            return run_gemm<GemmConfig<192, 4, B_MN, SB_VEC, EPI_BF16_TMA, 12>>(p, status, stream, dev);
     }
-    int cl = g_cluster.load(std::memory_order_relaxed);
-    if (cl == 0)
-        cl = 1;  // measured: multicast halves L2 traffic but the path is not L2-bound
-    if (cl == 2)
-        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 2>>(p, status, stream, dev);
     if (g_promo_warps.load(std::memory_order_relaxed) == 16)
-        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1, true, 16>>(p, status, stream, dev);
-    return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, 1>>(p, status, stream, dev);
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, EPI_BF16_TMA, 16>>(p, status, stream, dev);
+    return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC>>(p, status, stream, dev);
 }
 
 bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)
@@ -724,13 +672,6 @@ extern "C" int bfp8_set_gemm_promo_warps(int warps)
     if (warps != 8 && warps != 16)
         return BFP8_EINVAL;
     return g_promo_warps.exchange(warps);
-}
-
-extern "C" int bfp8_set_gemm_cluster(int cluster)
-{
-    if (cluster != 0 && cluster != 1 && cluster != 2)
-        return BFP8_EINVAL;
-    return g_cluster.exchange(cluster);
 }
 
 extern "C" int bfp8_set_gemm_tile_n(int tile_n)

@@ -60,12 +60,11 @@ namespace bfp8 {
 
 // Epilogue kinds: what the promotion warps do with a finished tile.
 enum GemmEpilogue {
-    EPI_BF16_DIRECT = 0,  // round to BF16, 16-byte stores straight from registers
-    EPI_BF16_TMA = 1,     // round to BF16, stage in shared memory, TMA store (default)
-    EPI_F32_ADD = 2,      // keep FP32, stage in shared memory, TMA reduce-add into an FP32 D
+    EPI_BF16_TMA = 1,  // round to BF16, stage in shared memory, TMA store (default)
+    EPI_F32_ADD = 2,   // keep FP32, stage in shared memory, TMA reduce-add into an FP32 D
 };
 
-template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int CLUSTER_ = 1, int EPI_ = EPI_BF16_TMA, int PW_ = 8>
+template <int BN_, int STAGES_, bool B_MN_, bool SB_VEC_, int EPI_ = EPI_BF16_TMA, int PW_ = 8>
 struct GemmConfig {
     static constexpr int BM = 128;
     static constexpr int BN = BN_;
@@ -76,16 +75,9 @@ struct GemmConfig {
     static constexpr bool B_MN = B_MN_;      // B stored MN-major (contraction axis strided)
     static constexpr bool SB_VEC = SB_VEC_;  // B scales per column (else per 128-column block)
     // epilogue: EPI_BF16_TMA stages BF16 tiles in shared memory and stores them
-    // with TMA; EPI_BF16_DIRECT has each thread store its row's 16-byte groups
-    // straight to global memory, which frees the staging slab for a deeper
-    // operand ring but measured slower (the uncoalesced stores hold up the
-    // promotion warps); EPI_F32_ADD stages FP32 boxes in the same slab and adds
-    // them into an FP32 D with TMA reduce-add (D += result, no BF16 rounding)
+    // with TMA; EPI_F32_ADD stages FP32 boxes in the same slab and adds them into
+    // an FP32 D with TMA reduce-add (D += result, no BF16 rounding)
     static constexpr int EPI = EPI_;
-    static constexpr bool EPI_SMEM = EPI_ != EPI_BF16_DIRECT;
-    // CTAs per cluster along M: the CTAs of a cluster compute vertically adjacent
-    // tiles that share one B tile; each loads 1/CLUSTER of it and multicasts it
-    static constexpr int CLUSTER = CLUSTER_;
     // Promotion warps: PW/4 column groups per TMEM lane quarter. More warps hide the
     // TMEM-load latency behind other warps' arithmetic; fewer leave more registers.
     static constexpr int PROMO_WARPS = PW_;
@@ -113,7 +105,7 @@ struct GemmConfig {
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
     // (64 BF16 or 32 FP32 columns; 4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
-    static constexpr int STAGE_OUT_BYTES = EPI_SMEM ? PROMO_WARPS * (CPW / 64) * BOX_BYTES : 0;
+    static constexpr int STAGE_OUT_BYTES = PROMO_WARPS * (CPW / 64) * BOX_BYTES;
     // shared-memory layout (offsets from a 1024-byte-aligned base)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -127,7 +119,6 @@ struct GemmConfig {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static_assert(BN == 128 || BN == 192 || BN == 256, "BN must be 128, 192 or 256");
     static_assert(BN != 192 || (!B_MN && CPW == 64), "192-wide tiles: K-major B, 64 columns per promotion warp");
-    static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN == 256), "clusters of 2 with 256-wide tiles only");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     // registers per thread at launch (65536 / THREADS, rounded down to a multiple of 8)
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
@@ -143,33 +134,26 @@ struct GemmArgs {
     int gm, gn, num_chunks;
     int tiles_m, tiles_n;
     int n_fastest;            // tile order: 1 = sweep the N tiles of a row block first
-    uint16_t* d;              // output (BF16) and its row stride in elements, for direct stores
-    int64_t ldd;
     const float* sb_scalar;   // scalar mode: sB(c, j) = sb_scalar[(j/128) * sb_col_stride + c * sb_chunk_stride]
     int64_t sb_col_stride, sb_chunk_stride;
     unsigned* status;
 };
 
-// Origin of the t-th tile of this CTA. Tiles are handed out in a static
-// round-robin over clusters; the CTAs of a cluster take vertically adjacent
-// tiles (same columns) of one "super tile" of CLUSTER x 1 tiles.
+// Origin of the t-th tile of this CTA: tiles are handed out in a static
+// round-robin over the CTAs.
 template <class Cfg>
 __device__ __forceinline__ void tile_origin(const GemmArgs& args, int t, int& m0, int& n0)
 {
-    const int nclusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
-    const int cid = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
-    const int rank = static_cast<int>(blockIdx.x) % Cfg::CLUSTER;
-    const int super_m = (args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER;
-    const int id = cid + t * nclusters;
-    int sm, nb;
+    const int id = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+    int mb, nb;
     if (args.n_fastest) {
         nb = id % args.tiles_n;
-        sm = id / args.tiles_n;
+        mb = id / args.tiles_n;
     } else {
-        sm = id % super_m;
-        nb = id / super_m;
+        mb = id % args.tiles_m;
+        nb = id / args.tiles_m;
     }
-    m0 = (sm * Cfg::CLUSTER + rank) * Cfg::BM;
+    m0 = mb * Cfg::BM;
     n0 = nb * Cfg::BN;
 }
 
@@ -201,18 +185,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nc = args.num_chunks;
-    // super tiles (CLUSTER x 1 tiles) handed out round-robin over the clusters
-    const int total_tiles = ((args.tiles_m + Cfg::CLUSTER - 1) / Cfg::CLUSTER) * args.tiles_n;
-    const int nclusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
-    const int cid = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
-    const uint32_t crank = Cfg::CLUSTER > 1 ? cluster_ctarank() : 0u;
-    const int my_tiles = total_tiles > cid ? (total_tiles - 1 - cid) / nclusters + 1 : 0;
+    // tiles handed out round-robin over the CTAs
+    const int total_tiles = args.tiles_m * args.tiles_n;
+    const int ncta = static_cast<int>(gridDim.x);
+    const int cta = static_cast<int>(blockIdx.x);
+    const int my_tiles = total_tiles > cta ? (total_tiles - 1 - cta) / ncta + 1 : 0;
     const int my_chunks = my_tiles * nc;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], Cfg::CLUSTER);  // one MMA completion per CTA of the cluster
+            mbar_init(&empty[s], 1);  // one MMA completion
         }
         for (int s = 0; s < Cfg::SSTAGES; ++s) {
             mbar_init(&sfull[s], 1);
@@ -232,8 +215,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmSA);
         if (Cfg::SB_VEC)
             tma_prefetch_desc(&tmSB);
-        if (Cfg::EPI_SMEM)
-            tma_prefetch_desc(&tmD);
+        tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
@@ -241,8 +223,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (Cfg::CLUSTER > 1)
-        cluster_sync();  // every CTA's barriers are initialised before any multicast reaches them
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -264,17 +244,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 mbar_arrive_expect_tx(&full[s], Cfg::OP_TX);
                 tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], c * Cfg::BK, m0);
-                if (Cfg::CLUSTER > 1) {
-                    // this CTA's share of the B tile goes to every CTA of the cluster
-                    constexpr uint16_t mask = (1u << Cfg::CLUSTER) - 1;
-                    constexpr int part = Cfg::BN / Cfg::CLUSTER;  // B rows (or MN columns) per CTA
-                    if (Cfg::B_MN)
-                        tma_load_2d_multicast(sB + s * Cfg::B_BYTES + crank * part * Cfg::BK, &tmB, &full[s],
-                                              n0 + crank * part, c * Cfg::BK, mask);
-                    else
-                        tma_load_2d_multicast(sB + s * Cfg::B_BYTES + crank * part * Cfg::BK, &tmB, &full[s],
-                                              c * Cfg::BK, n0 + crank * part, mask);
-                } else if (Cfg::B_MN) {
+                if (Cfg::B_MN) {
 #pragma unroll
                     for (int a = 0; a < Cfg::BN / 128; ++a)
                         tma_load_2d(sB + s * Cfg::B_BYTES + a * 128 * Cfg::BK, &tmB, &full[s], n0 + a * 128,
@@ -378,10 +348,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     asm("mov.b64 %0, {%1, %2};" : "=l"(bd) : "r"(b_lo + b_off + kk * kBStep), "r"(b_hi));
                     mma_e4m3(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
                 }
-                if (Cfg::CLUSTER > 1)
-                    mma_commit_multicast(&empty[s], (1u << Cfg::CLUSTER) - 1);  // the stage is free in every CTA
-                else
-                    mma_commit(&empty[s]);
+                mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
                 if (++s == Cfg::STAGES) {
                     s = 0;
@@ -524,7 +491,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             tma_store_commit();
                         }
                     }
-                } else if constexpr (Cfg::EPI == EPI_BF16_TMA) {
+                } else {
                     if (lane == 0)
                         tma_store_wait_read_all();  // this warp's previous stores have left the slab
                     __syncwarp();
@@ -551,21 +518,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                 tma_store_2d(&tmD, my_out + bx * Cfg::BOX_BYTES, col0 + bx * 64, m0 + quarter * 32);
                         tma_store_commit();
                     }
-                } else {
-                    const int grow = m0 + row;
-                    if (grow < args.gm && col0 < args.gn) {
-                        uint16_t* dst = args.d + static_cast<int64_t>(grow) * args.ldd + col0;
-#pragma unroll
-                        for (int k = 0; k < CPW / 8; ++k) {
-                            const uint64_t* v = acc + k * 4;
-                            uint4 pk;
-                            pk.x = cvt_bf16x2(v[0]);
-                            pk.y = cvt_bf16x2(v[1]);
-                            pk.z = cvt_bf16x2(v[2]);
-                            pk.w = cvt_bf16x2(v[3]);
-                            *reinterpret_cast<uint4*>(dst + 8 * k) = pk;
-                        }
-                    }
                 }
 #pragma unroll
                 for (int i = 0; i < CPW / 2; ++i)
@@ -575,14 +527,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tile_origin<Cfg>(args, t, m0, n0);
             }
         }
-        if (Cfg::EPI_SMEM && lane == 0)
+        if (lane == 0)
             tma_store_wait_read_all();
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (Cfg::CLUSTER > 1)
-        cluster_sync();  // no CTA leaves while a peer may still multicast into it or signal its barriers
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);

@@ -193,14 +193,6 @@ int bfp8_last_device_status(void* stream);
  * every thread. */
 int bfp8_set_gemm_tile_n(int tile_n);
 
-/* Tuning knob for the 256-wide GEMM tiles: 0 = automatic (default, currently
- * 1), 1 = one CTA per tile, 2 = clusters of two CTAs on vertically adjacent
- * tiles that share each B tile through TMA multicast (half the B traffic from
- * L2).
- * Returns the previous setting, or BFP8_EINVAL. Applies to later calls from
- * every thread. */
-int bfp8_set_gemm_cluster(int cluster);
-
 /* Tuning knob for the 256-wide GEMM tiles: promotion warps per CTA, 8
  * (default; 128 columns each) or 16 (64 columns each, more latency hiding,
  * fewer registers per thread). Returns the previous setting, or BFP8_EINVAL.

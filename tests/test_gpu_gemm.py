@@ -22,20 +22,17 @@ pytestmark = pytest.mark.gpu
 TILE = 128
 
 
-@pytest.fixture(params=[(128, 1, 8), (192, 1, 8), (256, 1, 8), (256, 2, 8), (256, 1, 16)],
-                ids=lambda p: f"tileN{p[0]}-cluster{p[1]}-warps{p[2]}")
+@pytest.fixture(params=[(128, 8), (192, 8), (256, 8), (256, 16)],
+                ids=lambda p: f"tileN{p[0]}-warps{p[1]}")
 def tile_n(request):
     """Every tile configuration: 128-wide tiles, 192-wide tiles with 12 promotion warps
     (forward and weight gradient; the input gradient then runs 256-wide), 256-wide
-    tiles one CTA each, 256-wide tiles in clusters of two CTAs sharing B through
-    multicast, and 256-wide tiles with 16 promotion warps."""
-    tn, cl, pw = request.param
+    tiles, and 256-wide tiles with 16 promotion warps."""
+    tn, pw = request.param
     prev_t = bfp8.set_gemm_tile_n(tn)
-    prev_c = bfp8.set_gemm_cluster(cl)
     prev_w = bfp8.set_gemm_promo_warps(pw)
     yield tn
     bfp8.set_gemm_tile_n(prev_t)
-    bfp8.set_gemm_cluster(prev_c)
     bfp8.set_gemm_promo_warps(prev_w)
 
 
