@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
         "fp8_block_gemm_wgrad_acc": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
         "bfp8_last_device_status": [p],
         "bfp8_set_gemm_tile_n": [c_int],
+        "bfp8_set_wait_limit_ns": [i64],
+        "bfp8_test_stall_producers": [c_int],
         "bfp8_set_gemm_promo_warps": [c_int],
         "muonh_partials_len": [ctypes.POINTER(c_int)],
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
@@ -237,6 +239,20 @@ def fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad):
 def last_device_status() -> int:
     """Synchronise the current stream and read/clear the kernels' bounded-wait status word."""
     return load_library().bfp8_last_device_status(_stream())
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of one in-kernel pipeline wait in ns (0 = the default 2 s)."""
+    _check("bfp8_set_wait_limit_ns", load_library().bfp8_set_wait_limit_ns(int(ns)))
+
+
+def test_stall_producers(on: bool) -> bool:
+    """Test switch: later quantiser and GEMM launches load nothing, so their waits run out.
+    Returns the previous setting."""
+    rc = load_library().bfp8_test_stall_producers(1 if on else 0)
+    if rc < 0:
+        raise ValueError("on must be a bool")
+    return bool(rc)
 
 
 def set_gemm_tile_n(tile_n: int) -> int:

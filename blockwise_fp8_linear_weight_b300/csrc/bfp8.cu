@@ -28,6 +28,8 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;  // TMA coordinates are in
 constexpr int64_t kMaxGridY = 65535;
 
 std::atomic<int> g_tile_n{0};
+std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
+std::atomic<int> g_stall{0};
 std::atomic<int> g_promo_warps{8};
 
 // ----------------------------------------------------------------- helpers
@@ -200,6 +202,8 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     args.sb_col_stride = p.sb_col_stride;
     args.sb_chunk_stride = p.sb_chunk_stride;
     args.status = status;
+    args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    args.stall = g_stall.load(std::memory_order_relaxed);
     // persistent grid: one CTA per SM, or one per tile if there are fewer tiles
     const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
     const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
@@ -275,6 +279,8 @@ int run_quant_blocks(const void* x, int64_t R, int64_t C, int64_t ldx, const Qua
     a.nblk_c = C / 128;
     a.nblocks = ((R + 127) / 128) * a.nblk_c;
     a.status = status;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.stall = g_stall.load(std::memory_order_relaxed);
     const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * 3);
     kern<<<static_cast<unsigned>(ctas), 256, kQuantSmemBytes, stream>>>(tm, a);
     return launch_status();
@@ -610,7 +616,8 @@ static int muonh_apply_impl(float* w, int64_t ldw, const void* u, int64_t ldu, i
         return BFP8_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* ub = static_cast<const uint16_t*>(u);
-    muonh_dot3_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials);
+    muonh_sumsq_u_kernel<<<grid, kMuonThreads, 0, st>>>(ub, ldu, rows, cols, partials);
+    muonh_wprime_sumsq_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
     muonh_apply_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
     return launch_status();
 }
@@ -672,6 +679,23 @@ extern "C" int bfp8_set_gemm_promo_warps(int warps)
     if (warps != 8 && warps != 16)
         return BFP8_EINVAL;
     return g_promo_warps.exchange(warps);
+}
+
+extern "C" int bfp8_set_wait_limit_ns(int64_t ns)
+{
+    if (ns == 0)
+        ns = static_cast<int64_t>(kWaitLimitNs);
+    if (ns < 1000 || ns > 60000000000ll)
+        return BFP8_EINVAL;
+    g_wait_ns.store(static_cast<unsigned long long>(ns), std::memory_order_relaxed);
+    return BFP8_OK;
+}
+
+extern "C" int bfp8_test_stall_producers(int on)
+{
+    if (on != 0 && on != 1)
+        return BFP8_EINVAL;
+    return g_stall.exchange(on);
 }
 
 extern "C" int bfp8_set_gemm_tile_n(int tile_n)

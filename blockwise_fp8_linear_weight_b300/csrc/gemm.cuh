@@ -137,6 +137,8 @@ struct GemmArgs {
     const float* sb_scalar;   // scalar mode: sB(c, j) = sb_scalar[(j/128) * sb_col_stride + c * sb_chunk_stride]
     int64_t sb_col_stride, sb_chunk_stride;
     unsigned* status;
+    unsigned long long wait_ns;  // limit of one mbarrier wait
+    int stall;                   // test switch: the operand producer issues no copies
 };
 
 // Origin of the t-th tile of this CTA: tiles are handed out in a static
@@ -237,10 +239,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int issued = 0;
             int t = 0, c = 0, m0 = 0, n0 = 0;
             tile_origin<Cfg>(args, 0, m0, n0);
-            for (int g = 0; g < my_chunks; ++g) {
+            // with the test switch on, nothing is loaded: the MMA issuer's first wait
+            // runs out, and every role unwinds through its bounded waits
+            const int to_issue = args.stall ? 0 : my_chunks;
+            for (int g = 0; g < to_issue; ++g) {
                 const int s = g % Cfg::STAGES;
                 const uint32_t ph = (g / Cfg::STAGES) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status))
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status, args.wait_ns))
                     break;
                 mbar_arrive_expect_tx(&full[s], Cfg::OP_TX);
                 tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], c * Cfg::BK, m0);
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // for the last phase of every stage that was filled
             volatile int never = 0;
             for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g)
-                mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status);
+                mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status, args.wait_ns);
         }
     } else if (warp == 2) {
         // ---------------------------------------------------------------- scale producer
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // leave the loop while the others reach the __syncwarp below
                 int ready = 1;
                 if (lane == 0)
-                    ready = mbar_wait(&sempty[qs], qph ^ 1, abort_flag, args.status) ? 1 : 0;
+                    ready = mbar_wait(&sempty[qs], qph ^ 1, abort_flag, args.status, args.wait_ns) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, ready, 0)) {
                     ok = false;
                     break;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0) {
             volatile int never = 0;
             for (int q = issued - Cfg::SSTAGES < 0 ? 0 : issued - Cfg::SSTAGES; q < issued; ++q)
-                mbar_wait(&sfull[q % Cfg::SSTAGES], (q / Cfg::SSTAGES) & 1, &never, args.status);
+                mbar_wait(&sfull[q % Cfg::SSTAGES], (q / Cfg::SSTAGES) & 1, &never, args.status, args.wait_ns);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -336,9 +341,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0, b = 0;
             uint32_t ph = 0, bph = 0, a_off = 0, b_off = 0, d_tmem = tmem_base;
             for (int g = 0; g < my_chunks; ++g) {
-                if (!mbar_wait(&full[s], ph, abort_flag, args.status))
+                if (!mbar_wait(&full[s], ph, abort_flag, args.status, args.wait_ns))
                     break;
-                if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, args.status))
+                if (!mbar_wait(&tempty[b], bph ^ 1, abort_flag, args.status, args.wait_ns))
                     break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // all issued MMAs must be complete before TMEM is released
             mma_commit(mma_done);
             volatile int never = 0;
-            mbar_wait(mma_done, 0, &never, args.status);
+            mbar_wait(mma_done, 0, &never, args.status, args.wait_ns);
         }
     }
     } else {
@@ -397,9 +402,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int g = 0; g < my_chunks; ++g) {
             const int b = g % Cfg::NBUF;
             const uint32_t bph = (g / Cfg::NBUF) & 1;
-            if (gi == 0 && !mbar_wait(&sfull[qs], qph, abort_flag, args.status))
+            if (gi == 0 && !mbar_wait(&sfull[qs], qph, abort_flag, args.status, args.wait_ns))
                 break;
-            if (!mbar_wait(&tfull[b], bph, abort_flag, args.status))
+            if (!mbar_wait(&tfull[b], bph, abort_flag, args.status, args.wait_ns))
                 break;
             tc_fence_after_sync();
             const int slot = qs * Cfg::SGROUP + gi;  // this chunk's row of the scale stage

@@ -12,8 +12,11 @@
 //   U     = Newton-Schulz iterations on X0       (plain BF16 GEMMs)
 //   W'    = W - lr R U / |U|                     (relative update size lr)
 //   W_new = R W' / |W'|                          (back onto the sphere |W| = R)
-// |W'|^2 = |W|^2 - 2 a <W,U> + a^2 |U|^2 with a = lr R / |U|, so one reduction
-// pass over (W, U) gives every norm and one more pass writes W_new.
+// Three passes: |U|^2 (reads U), then |W'|^2 of the FP32 W' = fma(-a, U, W)
+// that the last pass writes (reads W and U), then W_new (reads W and U, writes
+// W). Summing the squares of W' itself, rather than expanding |W'|^2 as
+// |W|^2 - 2 a <W,U> + a^2 |U|^2, keeps the norm free of cancellation: when W'
+// is exactly zero the sum is zero and W is left unchanged.
 //
 // Sums are deterministic: each CTA reduces a fixed set of rows (FP32 within a
 // row segment of a thread, FP64 beyond), warps by a fixed butterfly, CTAs by
@@ -122,71 +125,115 @@ __global__ void __launch_bounds__(kMuonThreads) muonh_scale_bf16_kernel(const fl
     }
 }
 
-// partials[blockIdx.x] = (sum w^2, sum w u, sum u^2) over the CTA's rows; w FP32, u BF16.
-__global__ void __launch_bounds__(kMuonThreads) muonh_dot3_kernel(const float* __restrict__ w, int64_t ldw,
-                                                                  const uint16_t* __restrict__ u, int64_t ldu,
-                                                                  int64_t rows, int64_t cols,
-                                                                  double* __restrict__ partials)
+// partials[blockIdx.x] = (0, 0, sum u^2) over the CTA's rows; u BF16 [rows][ldu].
+__global__ void __launch_bounds__(kMuonThreads) muonh_sumsq_u_kernel(const uint16_t* __restrict__ u, int64_t ldu,
+                                                                     int64_t rows, int64_t cols,
+                                                                     double* __restrict__ partials)
 {
     __shared__ double sh[kMuonThreads / 32][3];
-    double ww = 0.0, wu = 0.0, uu = 0.0;
+    double uu = 0.0, zero1 = 0.0, zero2 = 0.0;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-        const float4* wr = reinterpret_cast<const float4*>(w + r * ldw);
         const uint2* ur = reinterpret_cast<const uint2*>(u + r * ldu);
-        float sww = 0.0f, swu = 0.0f, suu = 0.0f;
+        float suu = 0.0f;
         for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
-            const float4 a = wr[j];
             const uint2 b = ur[j];
             const float u0 = bf16_to_f32(static_cast<uint16_t>(b.x)), u1 = bf16_to_f32(static_cast<uint16_t>(b.x >> 16));
             const float u2 = bf16_to_f32(static_cast<uint16_t>(b.y)), u3 = bf16_to_f32(static_cast<uint16_t>(b.y >> 16));
-            sww = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(a.z, a.z, fmaf(a.w, a.w, sww))));
-            swu = fmaf(a.x, u0, fmaf(a.y, u1, fmaf(a.z, u2, fmaf(a.w, u3, swu))));
             suu = fmaf(u0, u0, fmaf(u1, u1, fmaf(u2, u2, fmaf(u3, u3, suu))));
         }
-        ww += static_cast<double>(sww);
-        wu += static_cast<double>(swu);
         uu += static_cast<double>(suu);
     }
-    block_sum3(ww, wu, uu, sh);
+    block_sum3(uu, zero1, zero2, sh);
     if (threadIdx.x == 0) {
-        partials[3 * blockIdx.x + 0] = ww;
-        partials[3 * blockIdx.x + 1] = wu;
+        partials[3 * blockIdx.x + 0] = 0.0;
+        partials[3 * blockIdx.x + 1] = 0.0;
         partials[3 * blockIdx.x + 2] = uu;
     }
 }
 
-// w = R (w - a u) / |w - a u| with a = lr R / |u|, from the dot3 partials; in place.
-// |u| = 0 leaves the direction unchanged (a = 0); a zero W' leaves w unchanged.
+// Step coefficient a = lr R / |U| from the |U|^2 partials (component 2), 0 if |U| = 0.
+__device__ __forceinline__ float muonh_step_coef(const double* partials, int nparts, float lr, float radius)
+{
+    const double nu = sqrt(sum_partials(partials, nparts, 2));
+    return nu > 0.0 ? static_cast<float>(static_cast<double>(lr) * static_cast<double>(radius) / nu) : 0.0f;
+}
+
+// partials[blockIdx.x].0 = sum of W'^2 over the CTA's rows, W' = fma(-a, u, w) in FP32
+// exactly as muonh_apply_kernel forms it; components 1 and 2 are left as they are.
+__global__ void __launch_bounds__(kMuonThreads) muonh_wprime_sumsq_kernel(const float* __restrict__ w, int64_t ldw,
+                                                                          const uint16_t* __restrict__ u, int64_t ldu,
+                                                                          int64_t rows, int64_t cols,
+                                                                          double* __restrict__ partials, int nparts,
+                                                                          float lr, float radius)
+{
+    __shared__ double sh[kMuonThreads / 32][3];
+    __shared__ float coef;
+    if (threadIdx.x == 0)
+        coef = muonh_step_coef(partials, nparts, lr, radius);
+    __syncthreads();
+    const float a = coef;
+    double pp = 0.0, zero1 = 0.0, zero2 = 0.0;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float4* wr = reinterpret_cast<const float4*>(w + r * ldw);
+        const uint2* ur = reinterpret_cast<const uint2*>(u + r * ldu);
+        float spp = 0.0f;
+        for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
+            const float4 v = wr[j];
+            const uint2 b = ur[j];
+            const float p0 = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x)), v.x);
+            const float p1 = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x >> 16)), v.y);
+            const float p2 = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y)), v.z);
+            const float p3 = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y >> 16)), v.w);
+            spp = fmaf(p0, p0, fmaf(p1, p1, fmaf(p2, p2, fmaf(p3, p3, spp))));
+        }
+        pp += static_cast<double>(spp);
+    }
+    // every CTA has read the |U|^2 partials before any CTA writes its own component 0
+    // (they live in different words, so there is no overlap to order)
+    block_sum3(pp, zero1, zero2, sh);
+    if (threadIdx.x == 0)
+        partials[3 * blockIdx.x + 0] = pp;
+}
+
+// w = R W' / |W'| in place, W' = fma(-a, u, w), from the |U|^2 (component 2) and
+// |W'|^2 (component 0) partials. |U| = 0 gives a = 0 (w is only projected); if
+// W' is exactly zero (|W'|^2 = 0), w is left unchanged. The factor R / |W'| is
+// applied as a power of two times an FP32 value, so that it cannot overflow
+// even when |W'| is tiny; in the normal range this gives the bits of a single
+// multiplication by fl32(R / |W'|).
 __global__ void __launch_bounds__(kMuonThreads) muonh_apply_kernel(float* __restrict__ w, int64_t ldw,
                                                                    const uint16_t* __restrict__ u, int64_t ldu,
                                                                    int64_t rows, int64_t cols,
                                                                    const double* __restrict__ partials, int nparts,
                                                                    float lr, float radius)
 {
-    __shared__ float coef[2];  // a, scale
+    __shared__ float coef[3];  // a, 2^e, fl32(R / |W'| / 2^e)
+    __shared__ int keep;
     if (threadIdx.x == 0) {
-        const double sww = sum_partials(partials, nparts, 0);
-        const double swu = sum_partials(partials, nparts, 1);
-        const double suu = sum_partials(partials, nparts, 2);
-        const double nu = sqrt(suu);
-        const double a = nu > 0.0 ? static_cast<double>(lr) * static_cast<double>(radius) / nu : 0.0;
-        double n2 = sww - 2.0 * a * swu + a * a * suu;
-        n2 = n2 > 0.0 ? n2 : 0.0;
-        coef[0] = static_cast<float>(a);
-        coef[1] = n2 > 0.0 ? static_cast<float>(static_cast<double>(radius) / sqrt(n2)) : 1.0f;
+        coef[0] = muonh_step_coef(partials, nparts, lr, radius);
+        const double n2 = sum_partials(partials, nparts, 0);
+        keep = !(n2 > 0.0);
+        const double scale = keep ? 1.0 : static_cast<double>(radius) / sqrt(n2);
+        int e = 0;
+        frexp(scale, &e);
+        const double p2 = ldexp(1.0, e / 2);
+        coef[1] = static_cast<float>(p2);
+        coef[2] = static_cast<float>(scale / p2);
     }
     __syncthreads();
-    const float a = coef[0], scale = coef[1];
+    if (keep)
+        return;
+    const float a = coef[0], f1 = coef[1], f2 = coef[2];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         float4* wr = reinterpret_cast<float4*>(w + r * ldw);
         const uint2* ur = reinterpret_cast<const uint2*>(u + r * ldu);
         for (int64_t j = threadIdx.x; j < cols / 4; j += kMuonThreads) {
             float4 v = wr[j];
             const uint2 b = ur[j];
-            v.x = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x)), v.x) * scale;
-            v.y = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x >> 16)), v.y) * scale;
-            v.z = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y)), v.z) * scale;
-            v.w = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y >> 16)), v.w) * scale;
+            v.x = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x)), v.x) * f1 * f2;
+            v.y = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.x >> 16)), v.y) * f1 * f2;
+            v.z = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y)), v.z) * f1 * f2;
+            v.w = fmaf(-a, bf16_to_f32(static_cast<uint16_t>(b.y >> 16)), v.w) * f1 * f2;
             wr[j] = v;
         }
     }

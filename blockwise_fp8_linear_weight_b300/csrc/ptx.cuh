@@ -12,7 +12,8 @@ namespace bfp8 {
 // gives up on a wait. Read back (and cleared) by bfp8_last_device_status().
 constexpr unsigned kDevTimeout = 1u;
 
-// A single wait on an mbarrier phase gives up after this long (globaltimer ns).
+// Default limit of a single wait on an mbarrier phase (globaltimer ns); the
+// host may set another one per launch (bfp8_set_wait_limit_ns).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -64,10 +65,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up
 // (returns false) when `abort_flag` is raised by another warp, or after
-// kWaitLimitNs, in which case it raises `abort_flag` and records kDevTimeout
-// in `status`. Never spins without a limit.
+// limit_ns, in which case it raises `abort_flag` and records kDevTimeout in
+// `status`. Never spins without a limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status)
+                                          unsigned* status, unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -78,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if ((it & 15u) == 0) {
             if (*abort_flag)
                 return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(status, kDevTimeout);
                 return false;

@@ -323,6 +323,8 @@ struct QuantArgs {
     float* st;
     int64_t ldst;
     unsigned* status;
+    unsigned long long wait_ns;  // limit of one mbarrier wait
+    int stall;                   // test switch: no block is loaded
 };
 
 // Row pass over 8 row tiles per half-warp (1x128 tiles along the columns):
@@ -442,7 +444,11 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
     const int64_t stride = gridDim.x;
     const int my_blocks = a.nblocks > first ? static_cast<int>((a.nblocks - 1 - first) / stride + 1) : 0;
 
+    int issued = 0;            // thread 0: blocks whose copy was started
     auto issue = [&](int i) {  // thread 0: load my i-th block into buffer i & 1
+        if (a.stall)           // test switch: nothing is loaded, so the first wait runs out
+            return;
+        ++issued;
         const int64_t b = first + static_cast<int64_t>(i) * stride;
         const int64_t rb = b / a.nblk_c, cb = b - rb * a.nblk_c;
         uint64_t* bar = &full[i & 1];
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         const int64_t b = first + static_cast<int64_t>(i) * stride;
         const int64_t rb = b / a.nblk_c, cb = b - rb * a.nblk_c;
         // every thread takes the same decision, so no thread can be left at a barrier
-        if (!__syncthreads_and(mbar_wait(&full[i & 1], (i >> 1) & 1, &abort_flag, a.status)))
+        if (!__syncthreads_and(mbar_wait(&full[i & 1], (i >> 1) & 1, &abort_flag, a.status, a.wait_ns)))
             break;
         const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + (i & 1) * kQuantTileBytes);
 
@@ -530,8 +536,8 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
     // an aborted CTA must not exit while a copy may still land in its shared memory
     if (tid == 0 && i < my_blocks) {
         volatile int never = 0;
-        for (int k = i; k < my_blocks && k < i + 2; ++k)
-            mbar_wait(&full[k & 1], (k >> 1) & 1, &never, a.status);
+        for (int k = i; k < issued && k < i + 2; ++k)
+            mbar_wait(&full[k & 1], (k >> 1) & 1, &never, a.status, a.wait_ns);
     }
 }
 

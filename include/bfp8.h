@@ -161,9 +161,11 @@ int muonh_partials_len(int* n);
 int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64_t ldg, void* x, int64_t ldx,
                     double* partials, int64_t partials_len, float eps, void* stream);
 
-/* w = R (w - a u) / |w - a u| in place, a = lr R / |u| (a = 0 if |u| = 0; w is
- * left unchanged if w - a u is zero). The norm of w - a u comes from
- * |w|^2 - 2 a <w,u> + a^2 |u|^2, so w and u are read twice in all.
+/* w = R (w - a u) / |w - a u| in place, a = lr R / |u| (a = 0 if |u| = 0).
+ * w - a u is formed in FP32 as fma(-a, u, w), and its norm is the sum of the
+ * squares of exactly those values (FP32 within a row segment, FP64 beyond); if
+ * that sum is zero, w is left unchanged. Three passes: u is read three times,
+ * w twice, and w written once.
  *   w FP32 [rows][ldw] (16-byte aligned, ldw % 4 == 0), u BF16 [rows][ldu]
  *   (8-byte aligned, ldu % 4 == 0), lr >= 0, radius > 0.
  * Errors: as muonh_normalize (lr, radius checked as BFP8_EINVAL). */
@@ -185,6 +187,22 @@ const char* bfp8_status_string(int status);
  * kernel sets when it gives up on a bounded wait. Returns BFP8_OK,
  * BFP8_ETIMEOUT, or BFP8_ELAUNCH if the synchronisation itself failed. */
 int bfp8_last_device_status(void* stream);
+
+/* Limit of a single wait of a kernel on one of its own pipeline barriers, in
+ * nanoseconds of the GPU's global timer: 0 restores the default (2 s);
+ * otherwise 1000 <= ns <= 6e10. A kernel whose wait runs out records
+ * BFP8_ETIMEOUT in the device status word (read by bfp8_last_device_status),
+ * waits for its own copies in flight, releases its tensor memory and returns;
+ * its outputs are then unspecified. Applies to later launches from every
+ * thread. Returns BFP8_OK, or BFP8_EINVAL for a value out of range. */
+int bfp8_set_wait_limit_ns(int64_t ns);
+
+/* Test switch for the timeout path: with on = 1, later launches of the
+ * quantisers and GEMMs start no operand copies, so their first pipeline wait
+ * runs out (after the limit above) and the kernels unwind as described there.
+ * Meant for tests of the error path only; on = 0 (default) restores normal
+ * operation. Returns the previous setting (0 or 1), or BFP8_EINVAL. */
+int bfp8_test_stall_producers(int on);
 
 /* Tuning knob for the GEMMs' output tile width: 0 = automatic (default),
  * 128, 192 or 256 columns (192 applies to the forward and weight-gradient

@@ -25,7 +25,7 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
-                          "bfp8_set_gemm_promo_warps",
+                          "bfp8_set_gemm_promo_warps", "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers",
                           "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
@@ -45,6 +45,17 @@ def test_tile_knob(lib):
     assert lib.bfp8_set_gemm_promo_warps(12) == EINVAL
     prev = lib.bfp8_set_gemm_promo_warps(16)
     assert lib.bfp8_set_gemm_promo_warps(prev) == 16
+
+
+def test_wait_limit_and_stall_switch_arguments(lib):
+    assert lib.bfp8_set_wait_limit_ns(999) == EINVAL
+    assert lib.bfp8_set_wait_limit_ns(-1) == EINVAL
+    assert lib.bfp8_set_wait_limit_ns(60_000_000_001) == EINVAL
+    assert lib.bfp8_set_wait_limit_ns(1000) == OK
+    assert lib.bfp8_set_wait_limit_ns(0) == OK  # back to the default
+    assert lib.bfp8_test_stall_producers(2) == EINVAL
+    assert lib.bfp8_test_stall_producers(1) == 0
+    assert lib.bfp8_test_stall_producers(0) == 1
 
 
 def test_quantiser_argument_checks(lib):

@@ -96,3 +96,38 @@ def test_apply_static_scratch_matches_caller_scratch(shape):
     got = w2.cpu().numpy().astype(np.float64)
     rms = np.sqrt(np.mean(want ** 2))
     assert np.all(np.abs(got - want) <= 4e-6 * np.abs(want) + 4e-6 * rms)
+
+
+def _degenerate(delta):
+    """U = +-1 on 64 x 64 (|U| = 64), lr = 1/4, R = 2, so a = lr R / |U| = 2^-7 exactly, and
+    W = a U + delta a V with V ~ N(0, 1): W - a U is delta a V (exactly zero for delta = 0)."""
+    rng = np.random.default_rng(21)
+    U = np.where(rng.standard_normal((64, 64)) < 0, -1.0, 1.0).astype(np.float32)
+    V = rng.standard_normal((64, 64)).astype(np.float32)
+    W = (np.float32(2.0 ** -7) * U + np.float32(delta * 2.0 ** -7) * V).astype(np.float32)
+    return W, U, V
+
+
+@pytest.mark.parametrize("static", [False, True], ids=["caller-scratch", "static-scratch"])
+def test_apply_leaves_w_unchanged_when_the_step_cancels_it(static):
+    W, U, _ = _degenerate(0.0)
+    w = torch.from_numpy(W.copy()).cuda()
+    u = torch.from_numpy(U).to(torch.bfloat16).cuda()
+    (bfp8.muonh_apply_static if static else bfp8.muonh_apply)(w, u, 0.25, 2.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy(), W)
+    assert np.array_equal(ref.apply(W, U, 0.25, 2.0), W)
+
+
+def test_apply_projects_onto_the_sphere_under_near_cancellation():
+    """W - a U is 1e-3 of W: the norm of W' comes from W' itself, so the result lies on the
+    sphere |w| = R and points along V (FP32 forms W' with an error of about 2^-24 |a U|,
+    i.e. 6e-5 of |W'| here)."""
+    W, U, V = _degenerate(1e-3)
+    w = torch.from_numpy(W.copy()).cuda()
+    bfp8.muonh_apply(w, torch.from_numpy(U).to(torch.bfloat16).cuda(), 0.25, 2.0)
+    torch.cuda.synchronize()
+    got = w.cpu().numpy().astype(np.float64)
+    assert abs(np.linalg.norm(got) - 2.0) <= 1e-5 * 2.0
+    want = 2.0 * V / np.linalg.norm(V.astype(np.float64))
+    assert np.linalg.norm(got - want) <= 1e-3 * 2.0

@@ -68,3 +68,14 @@ def test_zero_learning_rate_is_a_projection():
 def test_normalize():
     G = np.random.default_rng(1).standard_normal((8, 12))
     assert abs(np.linalg.norm(muonh.normalize(G, eps=0.0)) - 1.0) < 1e-14
+
+
+def test_zero_step_result_leaves_w_unchanged():
+    """W = a U exactly (a = lr R / |U|): W - a U is zero, which has no direction to project;
+    the update leaves W as it is. U = +-1 on 64 x 64 has |U| = 64, so with lr = 1/4 and R = 2,
+    a = 2^-7 and every product is exact."""
+    U = np.where(np.random.default_rng(4).standard_normal((64, 64)) < 0, -1.0, 1.0)
+    W = 2.0 ** -7 * U
+    assert np.linalg.norm(W - (0.25 * 2.0 / np.linalg.norm(U)) * U) == 0.0
+    got = muonh.apply(W, U, 0.25, 2.0)
+    assert np.array_equal(got, W)
