@@ -53,7 +53,9 @@ def parse():
                    help="time eager launches instead of replays of the step captured in a CUDA graph")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the side measurements (cuBLAS BF16 comparator, FP32-accumulating wgrad, "
-                        "weight-quantisation reuse)")
+                        "weight-quantisation reuse, MuonH, other workloads)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads (attention, 28-layer stack, single linear, shape sweep)")
     p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 192, 256],
                    help="GEMM tile width (0: automatic)")
     p.add_argument("--gemm-promo-warps", type=int, default=0, choices=[0, 8, 16],
@@ -173,7 +175,7 @@ class OracleSample:
     run(r): for every linear, the quantisers on r-row slices of x, dy and W (x also
     transposed), the forward and input-gradient GEMMs on r output rows and the
     weight-gradient GEMM on r rows of dW (contracting over all M tokens).
-    Returns (seconds, GEMM flops of the sample).
+    Returns a dict with the seconds and work of the quantisers and of the GEMMs.
     """
 
     def __init__(self, work: wl.Workload):
@@ -193,34 +195,45 @@ class OracleSample:
 
     def run(self, r: int):
         o = self.oracle
-        flops = 0
-        t0 = time.perf_counter()
+        res = {"quant_s": 0.0, "quant_bytes": 0, "gemm_s": 0.0, "flops": 0}
+
+        def quant(fn, a, nbytes):
+            t = time.perf_counter()
+            fn(a)
+            res["quant_s"] += time.perf_counter() - t
+            res["quant_bytes"] += nbytes
+
+        def gemm(fn, *a, flops, **kw):
+            t = time.perf_counter()
+            fn(*a, **kw)
+            res["gemm_s"] += time.perf_counter() - t
+            res["flops"] += flops
+
         for lin, x, w, dy, (qx, sx, qw, sw, qdy, sdy, qdyt, sdyt, qxt, sxt) in self.data:
             rm = np.arange(min(r, lin.M))
             rn = np.arange(min(r, lin.N))
-            o.quantize_act(x[:rm.size])
-            o.quantize_weight(w[:(rn.size + 127) // 128 * 128])
-            o.gemm_fwd(qx, sx, qw, sw, rows=rm)
-            flops += 2 * rm.size * lin.N * lin.K
+            quant(o.quantize_act, x[:rm.size], quant_bytes(rm.size, lin.K))
+            wr = (rn.size + 127) // 128 * 128
+            quant(o.quantize_weight, w[:wr], quant_bytes(wr, lin.K))
+            gemm(o.gemm_fwd, qx, sx, qw, sw, rows=rm, flops=2 * rm.size * lin.N * lin.K)
             if "dgrad" in self.work.passes:
-                o.quantize_act(dy[:rm.size])
-                o.gemm_dgrad(qdy, sdy, qw, sw, rows=rm)
-                flops += 2 * rm.size * lin.N * lin.K
+                quant(o.quantize_act, dy[:rm.size], quant_bytes(rm.size, lin.N))
+                gemm(o.gemm_dgrad, qdy, sdy, qw, sw, rows=rm, flops=2 * rm.size * lin.N * lin.K)
             if "wgrad" in self.work.passes:
-                o.quantize_transpose(dy[:rm.size])
-                o.quantize_transpose(x[:rm.size])
-                o.gemm_wgrad(qdyt, sdyt, qxt, sxt, lin.M, rows=rn)
-                flops += 2 * rn.size * lin.M * lin.K
-        return time.perf_counter() - t0, flops
+                quant(o.quantize_transpose, dy[:rm.size], quant_bytes(rm.size, lin.N))
+                quant(o.quantize_transpose, x[:rm.size], quant_bytes(rm.size, lin.K))
+                gemm(o.gemm_wgrad, qdyt, sdyt, qxt, sxt, lin.M, rows=rn, flops=2 * rn.size * lin.M * lin.K)
+        res["s"] = res["quant_s"] + res["gemm_s"]
+        return res
 
     def calibrate(self, target_s: float):
         """Smallest power-of-two-ish row count whose run takes about target_s seconds."""
         r = 2
-        dt, fl = self.run(r)
-        while dt < target_s / 2 and r < 1 << 14:
-            r = int(min(r * max(2.0, 0.8 * target_s / max(dt, 1e-3)), 1 << 14))
-            dt, fl = self.run(r)
-        return r, dt, fl
+        res = self.run(r)
+        while res["s"] < target_s / 2 and r < 1 << 14:
+            r = int(min(r * max(2.0, 0.8 * target_s / max(res["s"], 1e-3)), 1 << 14))
+            res = self.run(r)
+        return r, res
 
     @staticmethod
     def cores():
@@ -229,15 +242,206 @@ class OracleSample:
         except AttributeError:
             return os.cpu_count()
 
-    def describe(self, r: int, dt: float) -> str:
-        return (f"oracle (FP64, OpenMP) on {r} output rows per GEMM pass of every linear of {self.work.name} "
-                f"plus the quantisers on {r}-row slices; {dt:.2f} s per sample")
+    def describe(self, r: int, s: float) -> str:
+        r = min(r, max(max(l.M, l.N) for l in self.work.linears))
+        return (f"oracle (FP64, OpenMP) on {r} output rows (at most) per GEMM pass of every linear of "
+                f"{self.work.name} plus the quantisers on {r}-row slices; {s:.2f} s per sample")
+
+
+def rates(res: dict) -> dict:
+    """The oracle's GEMM rate (TFLOPS over GEMM time) and quantiser rate (GB/s over quantiser
+    time), reported apart: in a small sample the quantisers' fixed cost (a whole 128-row weight
+    block per linear) weighs more than in a large one."""
+    return {"gemm_tflops": round(res["flops"] / max(res["gemm_s"], 1e-9) / 1e12, 6),
+            "quant_gbs": round(res["quant_bytes"] / max(res["quant_s"], 1e-9) / 1e9, 4),
+            "gemm_s": round(res["gemm_s"], 3), "quant_s": round(res["quant_s"], 3)}
 
 
 def cpu_oracle_sample(work: wl.Workload, target_s: float):
     s = OracleSample(work)
-    r, dt, fl = s.calibrate(target_s)
-    return fl / dt / 1e12, s.cores(), {"sample": s.describe(r, dt)}
+    r, res = s.calibrate(target_s)
+    return {"value": round(res["flops"] / res["s"] / 1e12, 6), "unit": UNIT, "cores": s.cores(),
+            "kind": "oracle", "sample": s.describe(r, res["s"]), **rates(res)}
+
+
+# ---------------------------------------------------------------------------- peaks
+MMA_PROBE_TFLOPS = 4500.0  # back-to-back tcgen05 FP8 MMAs measured alone on this pool's B300s
+
+
+def choose_peak(clocks: dict, peaks: dict, peak_src: str):
+    """FP8 dense peak for the roofline: the measured BF16 cuBLAS figure x the nominal FP8/BF16
+    ratio. The burst figure applies when the sampled clocks show the GPU at its maximum SM clock
+    with no power or thermal cap during the timed region; otherwise the sustained (power-capped)
+    figure does. Returns (peak, which, label)."""
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = any(r in clocks.get("reasons", []) for r in
+                 ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"))
+    at_max = sm is not None and mx is not None and sm >= 0.97 * mx
+    which = "burst" if (at_max and not capped) else "sustained"
+    key = "bf16_tflops" if which == "burst" else "bf16_tflops_sustained"
+    label = (f"{peak_src}: 2 x {key} ({peaks[key]}) [{which}: median SM clock {sm} of {mx} MHz, "
+             f"reasons {clocks.get('reasons', [])}], FP8/BF16 nominal dense ratio 2")
+    return FP8_OVER_BF16 * peaks[key], which, label
+
+
+# ---------------------------------------------------------------------------- GPU helpers
+def gpu_inputs(torch, lin: wl.Linear, dev):
+    """x, W, dy of one linear drawn on the GPU with torch's seeded generator, in the
+    distributions of workloads.py (N(0,1) activations, x50 on 8 random channels for
+    "outliers", N(0, 0.02^2) weights, N(0,1) output gradients). Used for the large side
+    configurations, where drawing tens of GB with numpy on the host would take minutes."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(lin.seed)
+    if lin.x_dist == "student_t3":
+        z = torch.randn((lin.M, lin.K), generator=g, device=dev)
+        c = torch.randn((3, lin.M, lin.K), generator=g, device=dev).square().sum(0) / 3.0
+        x = z / c.sqrt()
+    else:
+        x = torch.randn((lin.M, lin.K), generator=g, device=dev)
+        if lin.x_dist == "outliers":
+            ch = torch.randperm(lin.K, generator=g, device=dev)[:8]
+            x[:, ch] *= 50.0
+    g.manual_seed(lin.seed + 1)
+    w = torch.randn((lin.N, lin.K), generator=g, device=dev) * 0.02
+    g.manual_seed(lin.seed + 2)
+    dy = torch.randn((lin.M, lin.N), generator=g, device=dev)
+    return x.to(torch.bfloat16), w.to(torch.bfloat16), dy.to(torch.bfloat16)
+
+
+class Case:
+    """Buffers and call sequence of one workload: a BlockwiseFP8Linear per distinct shape
+    (shared by linears of the same shape, as the layers of a stack run one after another)
+    and the inputs of every linear."""
+
+    def __init__(self, bfp8, torch, work: wl.Workload, dev, source: str = "numpy"):
+        self.bfp8, self.torch, self.work = bfp8, torch, work
+        self.fwd_only = work.passes == ("fwd",)
+        self.layers, self.inputs, by_shape = [], [], {}
+        for lin in work.linears:
+            key = (lin.M, lin.K, lin.N)
+            if key not in by_shape:
+                by_shape[key] = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev)
+            self.layers.append(by_shape[key])
+            if source == "numpy":
+                self.inputs.append(tuple(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+                                         for a in wl.make_linear(lin)))
+            else:
+                self.inputs.append(gpu_inputs(torch, lin, dev))
+
+    @property
+    def kernels_per_step(self):
+        return sum(3 if self.fwd_only else L.KERNELS_PER_STEP for L in self.layers)
+
+    def step(self, mark=None):
+        """One training step of every linear; mark(tag, work) after each kernel if given."""
+        b = self.bfp8
+        mark = mark or (lambda tag, work: None)
+        for L, (x, w, dy), lin in zip(self.layers, self.inputs, self.work.linears):
+            M, K, N = lin.M, lin.K, lin.N
+            if self.fwd_only:
+                b.fp8_quantize_act(x, L.qx, L.sx)
+                mark("quant_act", quant_bytes(M, K))
+            else:
+                b.fp8_quantize_act_transpose(x, L.qx, L.sx, L.qxt, L.sxt)
+                mark("quant_act_transpose", dual_bytes(M, K))
+            b.fp8_quantize_weight(w, L.qw, L.sw)
+            mark("quant_weight", quant_bytes(N, K))
+            b.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+            mark("gemm_fwd", 2 * M * N * K)
+            if self.fwd_only:
+                continue
+            b.fp8_quantize_act_transpose(dy, L.qdy, L.sdy, L.qdyt, L.sdyt)
+            mark("quant_act_transpose", dual_bytes(M, N))
+            b.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
+            mark("gemm_dgrad", 2 * M * N * K)
+            b.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw)
+            mark("gemm_wgrad", 2 * M * N * K)
+
+
+def capture(torch, fn):
+    """fn's launches captured in a CUDA graph (after one run on a side stream, so that the
+    library's lazily initialised state is set before capture). Every kernel is then launched
+    from the graph: host launch overhead (argument checks, tensor-map encoding, ctypes) leaves
+    the critical path."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_ms(torch, graph, n: int, stream) -> float:
+    """Device time of n back-to-back replays of a graph (CUDA events on the launching stream)."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_breakdown(torch, case: Case, steps: int, fp8_peak: float, hbm_peak: float, stream):
+    """Per-kernel device times of `steps` training steps captured in one CUDA graph with an
+    event node after every kernel, replayed once after a warm replay: kernels run back to back
+    exactly as in the timed graph, so no host launch gap enters a kernel's time. Returns
+    (kernels, total ms of the breakdown graph, source)."""
+    marks = []
+
+    def mark(tag=None, work=0):
+        e = torch.cuda.Event(enable_timing=True, external=True)
+        e.record()
+        marks.append((e, tag, work))
+
+    def body():
+        marks.clear()
+        mark()
+        for _ in range(steps):
+            case.step(mark)
+
+    g = capture(torch, body)
+    g.replay()
+    torch.cuda.synchronize()
+    per = {}
+    for (e0, _, _), (e1, tag, w) in zip(marks[:-1], marks[1:]):
+        k = per.setdefault(tag, {"launches": 0, "ms": 0.0, "work": 0})
+        k["launches"] += 1
+        k["ms"] += e0.elapsed_time(e1)
+        k["work"] += w
+    total = marks[0][0].elapsed_time(marks[-1][0])
+    kernels = {}
+    for tag, k in per.items():
+        gemm = tag.startswith("gemm")
+        rate = k["work"] / (k["ms"] / 1e3) / (1e12 if gemm else 1e9)
+        kernels[tag] = {"launches": k["launches"], "ms_total": round(k["ms"], 4),
+                        "avg_us": round(1e3 * k["ms"] / k["launches"], 2),
+                        ("tflops" if gemm else "gbs"): round(rate, 1),
+                        "frac_of_peak": round(rate / (fp8_peak if gemm else hbm_peak), 4),
+                        "share_of_step": round(k["ms"] / total, 4)}
+    return kernels, total
+
+
+def measure_case(torch, case: Case, steps: int, warmup: int, fp8_peak: float, hbm_peak: float, stream):
+    """Step throughput (graph replays) and the per-kernel breakdown of one workload."""
+    for _ in range(max(warmup, 1)):
+        case.step()
+    torch.cuda.synchronize()
+    g = capture(torch, case.step)
+    ms = replay_ms(torch, g, steps, stream)
+    kernels, bd_ms = kernel_breakdown(torch, case, min(steps, 20), fp8_peak, hbm_peak, stream)
+    flops = case.work.flops
+    return {"tflops": round(flops * steps / (ms / 1e3) / 1e12, 2), "ms_per_step": round(ms / steps, 5),
+            "frac_of_fp8_peak": round(flops * steps / (ms / 1e3) / 1e12 / fp8_peak, 4), "steps": steps,
+            "kernels": kernels}
 
 
 # ---------------------------------------------------------------------------- GPU arm
@@ -255,126 +459,52 @@ def run_ours(args):
 
     work = workload(args.workload)
     dev = torch.device("cuda", local)
-
-    def up(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    layers, inputs, host = [], [], []
-    for lin in work.linears:
-        x, w, dy = wl.make_linear(lin)
-        layers.append(bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev))
-        inputs.append((up(x), up(w), up(dy)))
-        if not args.no_e2e:
+    case = Case(bfp8, torch, work, dev)
+    host = []
+    if not args.no_e2e:
+        for lin in work.linears:
             host.append(tuple(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
-                              for a in (x, w, dy)))
-    fwd_only = work.passes == ("fwd",)
-
-    def step():
-        for L, (x, w, dy) in zip(layers, inputs):
-            if fwd_only:
-                bfp8.fp8_quantize_act(x, L.qx, L.sx)
-                bfp8.fp8_quantize_weight(w, L.qw, L.sw)
-                bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
-            else:
-                L.forward(x, w)
-                L.backward(dy)
-
-    kernels_per_step = sum(3 if fwd_only else L.KERNELS_PER_STEP for L in layers)
+                              for a in wl.make_linear(lin)))
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        step()
+        case.step()
     torch.cuda.synchronize()
     assert bfp8.last_device_status() == 0, "a kernel timed out during warm-up"
 
     # ------------------------------------------------------------ timed region
-    # One CUDA event between consecutive kernels on the launching stream: the
-    # difference of neighbouring events is that kernel's device time, and the
-    # first and last events bracket the whole timed region.
-    marks = []  # (event, tag, work) of the kernel that ended at this event
-
-    def mark(tag=None, work=0):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)
-        marks.append((e, tag, work))
-
-    def timed_step():
-        for L, (x, w, dy), lin in zip(layers, inputs, work.linears):
-            M, K, N = lin.M, lin.K, lin.N
-            if fwd_only:
-                bfp8.fp8_quantize_act(x, L.qx, L.sx)
-                mark("quant_act", quant_bytes(M, K))
-            else:
-                bfp8.fp8_quantize_act_transpose(x, L.qx, L.sx, L.qxt, L.sxt)
-                mark("quant_act_transpose", dual_bytes(M, K))
-            bfp8.fp8_quantize_weight(w, L.qw, L.sw)
-            mark("quant_weight", quant_bytes(N, K))
-            bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
-            mark("gemm_fwd", 2 * M * N * K)
-            if fwd_only:
-                continue
-            bfp8.fp8_quantize_act_transpose(dy, L.qdy, L.sdy, L.qdyt, L.sdyt)
-            mark("quant_act_transpose", dual_bytes(M, N))
-            bfp8.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
-            mark("gemm_dgrad", 2 * M * N * K)
-            bfp8.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw)
-            mark("gemm_wgrad", 2 * M * N * K)
-
-    # The timed region replays the step captured once in a CUDA graph (host launch
-    # overhead off the critical path); a following eager pass with one event between
-    # consecutive kernels gives the per-kernel breakdown.
-    graph = None if args.no_graph else capture_step(torch, step)
+    # K replays of one training step captured in a CUDA graph (host launch overhead off the
+    # critical path), bracketed by a barrier and a synchronize on both sides; --no-graph
+    # times K eager steps instead.
+    graph = None if args.no_graph else capture(torch, case.step)
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(ws)
         torch.cuda.synchronize()
-        if graph is not None:
-            g0.record(stream)
-            for _ in range(args.steps):
+        g0.record(stream)
+        for _ in range(args.steps):
+            if graph is not None:
                 graph.replay()
-            g1.record(stream)
-        else:
-            mark()
-            for _ in range(args.steps):
-                timed_step()
+            else:
+                case.step()
+        g1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
     clocks = clk.result()
-    if graph is not None:
-        ms_local = g0.elapsed_time(g1)
-        breakdown_steps = min(args.steps, 200)
-        torch.cuda.synchronize()
-        mark()
-        for _ in range(breakdown_steps):
-            timed_step()
-        torch.cuda.synchronize()
-        breakdown_ms = marks[0][0].elapsed_time(marks[-1][0])
-    else:
-        ms_local = marks[0][0].elapsed_time(marks[-1][0])
-        breakdown_steps, breakdown_ms = args.steps, ms_local
+    ms_local = g0.elapsed_time(g1)
     status = bfp8.last_device_status()
     ms = allreduce_max(ms_local, ws, dev)
     tflops = job_tflops(work.flops, args.steps, ws, ms)
 
     peaks, peak_src = measured_peaks()
-    # A kernel timed inside a long step: the sustained (power-capped) figures.
-    fp8_peak = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    fp8_peak, peak_kind, peak_label = choose_peak(clocks, peaks, peak_src)
+    fp8_burst = FP8_OVER_BF16 * peaks["bf16_tflops"]
+    fp8_sustained = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
     hbm_peak = peaks["hbm_gbs"]
-    per_kernel = {}
-    for (e0, _, _), (e1, tag, w) in zip(marks[:-1], marks[1:]):
-        k = per_kernel.setdefault(tag, {"launches": 0, "ms": 0.0, "work": 0})
-        k["launches"] += 1
-        k["ms"] += e0.elapsed_time(e1)
-        k["work"] += w
-    kernels = {}
-    for tag, k in per_kernel.items():
-        gemm = tag.startswith("gemm")
-        rate = k["work"] / (k["ms"] / 1e3) / (1e12 if gemm else 1e9)
-        kernels[tag] = {"launches": k["launches"], "ms_total": round(k["ms"], 3),
-                        "avg_us": round(1e3 * k["ms"] / k["launches"], 2),
-                        ("tflops" if gemm else "gbs"): round(rate, 1),
-                        "frac_of_peak": round(rate / (fp8_peak if gemm else hbm_peak), 4),
-                        "share_of_step": round(k["ms"] / breakdown_ms, 4)}
+
+    # per-kernel times: the same kernels replayed from a graph with event nodes between them
+    bd_steps = min(args.steps, 20)
+    kernels, bd_ms = kernel_breakdown(torch, case, bd_steps, fp8_peak, hbm_peak, stream)
     dom = max(kernels, key=lambda t: kernels[t]["ms_total"])
     gemm_dom = dom.startswith("gemm")
     achieved = kernels[dom]["tflops" if gemm_dom else "gbs"]
@@ -388,111 +518,47 @@ def run_ours(args):
     roofline = {"bound": "tensor" if gemm_dom else "hbm", "kernel": dom, "achieved": achieved,
                 "peak": round(fp8_peak if gemm_dom else hbm_peak, 1), "unit": "TFLOP/s" if gemm_dom else "GB/s",
                 "frac": round(kernels[dom]["frac_of_peak"], 4), "traffic": traffic,
-                "peak_source": (f"{peak_src}: 2 x bf16_tflops_sustained ({peaks['bf16_tflops_sustained']}), "
-                                f"FP8/BF16 nominal dense ratio 2" if gemm_dom else
-                                f"{peak_src}: hbm_gbs ({hbm_peak})")}
+                "peak_source": peak_label if gemm_dom else f"{peak_src}: hbm_gbs ({hbm_peak})"}
+    if gemm_dom:
+        roofline["frac_of_burst"] = round(achieved / fp8_burst, 4)
+        roofline["frac_of_sustained"] = round(achieved / fp8_sustained, 4)
+        roofline["frac_of_mma_probe"] = round(achieved / MMA_PROBE_TFLOPS, 4)
+        roofline["mma_probe_peak"] = {"tflops": MMA_PROBE_TFLOPS,
+                                      "what": "back-to-back tcgen05 FP8 MMAs (M=128, K=32) measured alone, "
+                                              "8180 MAC/clk/SM at an unthrottled clock"}
+    breakdown = {"steps": bd_steps, "ms_per_step": round(bd_ms / bd_steps, 5),
+                 "what": "the timed step's kernels replayed from one CUDA graph with an event node after "
+                         "every kernel; kernels and roofline come from this replay"}
 
     extras = None
     if not args.no_extras:
-        extras = {} if fwd_only else side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak,
-                                                        tflops, min(args.steps, 200), dev)
-    eager = {"tflops": round(work.flops * breakdown_steps / (breakdown_ms / 1e3) / 1e12, 2),
-             "ms_per_step": round(breakdown_ms / breakdown_steps, 5), "steps": breakdown_steps,
-             "what": "the same step launched eagerly from Python, one event between kernels (per-kernel "
-                     "breakdown and roofline come from this pass)"}
+        extras = {} if case.fwd_only else side_measurements(bfp8, torch, case, stream, fp8_peak, tflops,
+                                                             min(args.steps, 200), dev)
+        if not args.no_configs:
+            extras["configs"] = other_configs(bfp8, torch, args, work, dev, stream, fp8_peak, hbm_peak)
 
-    # ------------------------------------------------------------ end to end (host buffers)
-    # Every step copies x, W and dy of every linear in from pinned host memory and
-    # y, dx and dW out, through the public API. Copies in, compute and copies out
-    # run on three streams ordered by events, with two buffer sets per linear, so
-    # the copies of one linear overlap the kernels of another.
-    e2e = None
-    if not args.no_e2e:
-        sets = [[(tuple(torch.empty_like(t, device=dev) for t in h),
-                  bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev) if k else L)
-                 for h, lin, L in zip(host, work.linears, layers)] for k in range(2)]
-        outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.y, L.dx, L.dw))
-                     for L in layers]
-        bi = sum(t.numel() * 2 for h in host for t in h)
-        bo = sum(t.numel() * 2 for L in layers for t in ((L.y,) if fwd_only else (L.y, L.dx, L.dw)))
-        e2e_steps = max(3, min(args.steps, 50))
-        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        nl = len(layers)
-        ev_in = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
-        ev_cmp = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
-        ev_out = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
-        started = [[False] * nl for _ in range(2)]
-
-        def e2e_step(k):
-            p = k & 1
-            for i, (h, o) in enumerate(zip(host, outs_host)):
-                d, L = sets[p][i]
-                with torch.cuda.stream(s_in):
-                    if started[p][i]:
-                        s_in.wait_event(ev_cmp[p][i])  # the previous use of this input set is done
-                    for src, dst in zip(h, d):
-                        dst.copy_(src, non_blocking=True)
-                    ev_in[p][i].record(s_in)
-                with torch.cuda.stream(s_cmp):
-                    s_cmp.wait_event(ev_in[p][i])
-                    if started[p][i]:
-                        s_cmp.wait_event(ev_out[p][i])  # its outputs have been copied out
-                    if fwd_only:
-                        bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
-                        bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
-                        bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
-                    else:
-                        L.forward(d[0], d[1])
-                        L.backward(d[2])
-                    ev_cmp[p][i].record(s_cmp)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_cmp[p][i])
-                    o[0].copy_(L.y, non_blocking=True)
-                    if not fwd_only:
-                        o[1].copy_(L.dx, non_blocking=True)
-                        o[2].copy_(L.dw, non_blocking=True)
-                    ev_out[p][i].record(s_out)
-                started[p][i] = True
-
-        for k in range(2):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        barrier(ws)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(s_in)
-        for k in range(e2e_steps):
-            e2e_step(k)
-        s_out.wait_stream(s_in)
-        s_out.wait_stream(s_cmp)
-        s1.record(s_out)
-        torch.cuda.synchronize()
-        e2e_ms = allreduce_max(s0.elapsed_time(s1), ws, dev)
-        e2e = {"value": round(work.flops * e2e_steps * ws / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
-               "how": ("pinned host x, W, dy copied in and y, dx, dW copied out every step; copies in, "
-                       "compute and copies out on three streams ordered by events, two buffer sets per linear")}
+    e2e = None if args.no_e2e else end_to_end(bfp8, torch, case, host, dev, ws, args.steps)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, info = cpu_oracle_sample(work, args.cpu_seconds)
-        cpu = {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": info["sample"]}
+        cpu = cpu_oracle_sample(work, args.cpu_seconds)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(tflops, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-            "pct_of_fp8_peak": round(100 * tflops / fp8_peak, 2),
+            "pct_of_fp8_peak": round(100 * tflops / fp8_peak, 2), "fp8_peak_used": peak_kind,
+            "pct_of_fp8_burst_peak": round(100 * tflops / fp8_burst, 2),
             "config": {"workload": work.name, "linears": [f"{l.name}: M={l.M} K={l.K} N={l.N} x~{l.x_dist}"
                                                           for l in work.linears],
                        "passes": "+".join(work.passes) + " incl. all quantisers",
                        "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (no flush)",
                        "timing": ("eager launches" if args.no_graph else
                                   "one step captured in a CUDA graph, replayed K times")},
-            "roofline": roofline, "kernels": kernels, "eager_step": eager, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kernels": kernels, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,
             "extras": extras,
-            "gpu_launches": kernels_per_step * args.steps, "clocks": clocks,
+            "gpu_launches": case.kernels_per_step * args.steps, "clocks": clocks,
             "device_status": bfp8.STATUS.get(status, status),
         }
         print(json.dumps(line))
@@ -501,28 +567,117 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def capture_step(torch, step):
-    """One training step captured in a CUDA graph. Every kernel of the step is then launched
-    from the graph, so host launch overhead (argument checks, tensor-map encoding, ctypes)
-    leaves the critical path; small workloads are launch-bound without it. The library's
-    lazily initialised state (function attributes, device queries) is set by the warm-up
-    steps before capture."""
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        step()
-    torch.cuda.current_stream().wait_stream(side)
+def end_to_end(bfp8, torch, case: Case, host, dev, ws: int, steps: int):
+    """The metric through the public API with host buffers. Every step copies x, W and dy of
+    every linear in from pinned host memory and y, dx and dW out. Copies in, compute and copies
+    out run on three streams ordered by events, with two buffer sets per linear, so the copies
+    of one linear overlap the kernels of another."""
+    work, layers = case.work, case.layers
+    fwd_only = case.fwd_only
+    sets = [[(tuple(torch.empty_like(t, device=dev) for t in h),
+              bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev) if k else L)
+             for h, lin, L in zip(host, work.linears, layers)] for k in range(2)]
+    outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.y, L.dx, L.dw))
+                 for L in layers]
+    bi = sum(t.numel() * 2 for h in host for t in h)
+    bo = sum(t.numel() * 2 for L in layers for t in ((L.y,) if fwd_only else (L.y, L.dx, L.dw)))
+    e2e_steps = max(3, min(steps, 50))
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nl = len(layers)
+    ev_in = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+    ev_cmp = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(nl)] for _ in range(2)]
+    started = [[False] * nl for _ in range(2)]
+
+    def e2e_step(k):
+        p = k & 1
+        for i, (h, o) in enumerate(zip(host, outs_host)):
+            d, L = sets[p][i]
+            with torch.cuda.stream(s_in):
+                if started[p][i]:
+                    s_in.wait_event(ev_cmp[p][i])  # the previous use of this input set is done
+                for src, dst in zip(h, d):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[p][i].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[p][i])
+                if started[p][i]:
+                    s_cmp.wait_event(ev_out[p][i])  # its outputs have been copied out
+                if fwd_only:
+                    bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
+                    bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
+                    bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+                else:
+                    L.forward(d[0], d[1])
+                    L.backward(d[2])
+                ev_cmp[p][i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[p][i])
+                o[0].copy_(L.y, non_blocking=True)
+                if not fwd_only:
+                    o[1].copy_(L.dx, non_blocking=True)
+                    o[2].copy_(L.dw, non_blocking=True)
+                ev_out[p][i].record(s_out)
+            started[p][i] = True
+
+    for k in range(2):
+        e2e_step(k)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    for _ in range(3):
-        g.replay()
+    barrier(ws)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(s_in)
+    for k in range(e2e_steps):
+        e2e_step(k)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    s1.record(s_out)
     torch.cuda.synchronize()
-    return g
+    e2e_ms = allreduce_max(s0.elapsed_time(s1), ws, dev)
+    return {"value": round(work.flops * e2e_steps * ws / (e2e_ms / 1e3) / 1e12, 2), "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+            "how": ("pinned host x, W, dy copied in and y, dx, dW copied out every step; copies in, "
+                    "compute and copies out on three streams ordered by events, two buffer sets per linear")}
 
 
-def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_tflops, steps, dev):
+def other_configs(bfp8, torch, args, headline: wl.Workload, dev, stream, fp8_peak, hbm_peak):
+    """The other Puro-2B workloads, each timed like the headline (graph replays, per-kernel
+    breakdown from the graph with event nodes): the attention projections at M=4096, the
+    28-layer stack at M=16384 with outlier channels, the single 256^3 linear (forward only),
+    and the shape sweep (every M x (K, N) point). Inputs are drawn on the GPU (gpu_inputs)."""
+    out = {}
+    steps = max(3, min(args.steps, 50))
+    todo = [("attn", wl.attention_projections()), ("single", wl.single_linear_256()),
+            ("stack", wl.full_stack())]
+    for key, w in todo:
+        if w.name == headline.name:
+            continue
+        c = Case(bfp8, torch, w, dev, source="torch")
+        r = measure_case(torch, c, max(3, min(steps, 10)) if key == "stack" else steps, 2, fp8_peak,
+                         hbm_peak, stream)
+        r["workload"] = w.name
+        out[key] = r
+        del c
+        torch.cuda.empty_cache()
+    sweep = {}
+    for lin in wl.shape_sweep():
+        w = wl.Workload(lin.name, (lin,))
+        c = Case(bfp8, torch, w, dev, source="torch")
+        r = measure_case(torch, c, steps, 2, fp8_peak, hbm_peak, stream)
+        sweep[lin.name] = {"tflops": r["tflops"], "ms_per_step": r["ms_per_step"],
+                           "frac_of_fp8_peak": r["frac_of_fp8_peak"],
+                           "kernels": {k: v.get("tflops", v.get("gbs")) for k, v in r["kernels"].items()}}
+        del c
+        torch.cuda.empty_cache()
+    out["sweep"] = sweep
+    out["what"] = ("each workload's training step (all quantisers and GEMMs) replayed from a CUDA graph; "
+                   "kernels: per-kernel TFLOPS (GEMMs) or GB/s (quantisers) from a graph replay with event "
+                   "nodes; inputs drawn on the GPU with torch's seeded generator in the workloads' "
+                   "distributions")
+    return out
+
+
+def side_measurements(bfp8, torch, case: Case, stream, fp8_peak, fp8_tflops, steps, dev):
     """Measurements next to the headline number, outside its timed region (CUDA events,
     3 warm-up steps each, same inputs):
       bf16_cublas: the same three GEMMs per linear in BF16 through torch.matmul (cuBLAS), the
@@ -532,8 +687,9 @@ def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_t
       weight_quant_reuse: the training step of a micro-batch after the first, W's codes reused
         (five kernels per linear);
       muonh: one MuonH optimizer step on every linear's weight (FP32 master copy, N(0,1)
-        gradient): the library's normalise and apply kernels around five BF16 Newton-Schulz
-        iterations (cuBLAS GEMMs); rate = the iterations' GEMM FLOP over the whole update."""
+        gradient); rate = the Newton-Schulz iterations' GEMM FLOP over the whole update."""
+    work, layers, inputs = case.work, case.layers, case.inputs
+
     def timed(fn, n):
         for _ in range(3):
             fn()
@@ -564,7 +720,8 @@ def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_t
     out["bf16_cublas"] = {"tflops": round(bf16_tflops, 1), "ms_per_step": round(ms_bf16, 4),
                           "fp8_speedup": round(fp8_tflops / bf16_tflops, 3),
                           "what": "torch.matmul BF16 (cuBLAS) for fwd, dgrad and wgrad of every linear, "
-                                  "no quantisers; fp8_speedup = FP8 step (quantisers included) over this"}
+                                  "no quantisers, eager launches; fp8_speedup = FP8 step (quantisers "
+                                  "included) over this"}
 
     # wgrad into an FP32 main gradient, one launch per linear
     mgs = [torch.zeros((l.N, l.K), dtype=torch.float32, device=dev) for l in work.linears]
@@ -573,35 +730,40 @@ def side_measurements(bfp8, torch, work, layers, inputs, stream, fp8_peak, fp8_t
         for L, l, mg in zip(layers, work.linears, mgs):
             bfp8.fp8_block_gemm_wgrad_acc(L.qdyt, L.sdyt, L.qxt, L.sxt, l.M, mg)
 
-    ms_acc = timed(acc_step, steps)
+    g = capture(torch, acc_step)
+    ms_acc = replay_ms(torch, g, steps, stream) / steps
     acc_tflops = sum(2 * l.M * l.N * l.K for l in work.linears) / (ms_acc / 1e3) / 1e12
     out["wgrad_fp32_acc"] = {"tflops": round(acc_tflops, 1), "frac_of_peak": round(acc_tflops / fp8_peak, 4),
-                             "avg_us_per_launch": round(1e3 * ms_acc / len(layers), 2)}
+                             "avg_us_per_launch": round(1e3 * ms_acc / len(layers), 2),
+                             "what": "graph replays, one launch per linear"}
 
     # micro-batches after the first: W unchanged, its codes reused
     for L in layers:
         L.reuse_weight_quant = True
         L.invalidate_weight_quant()
+    case.step()  # quantises W once
+    torch.cuda.synchronize()
 
     def reuse_step():
         for L, (x, w, dy) in zip(layers, inputs):
             L.forward(x, w)
             L.backward(dy)
 
-    ms_reuse = timed(reuse_step, steps)
+    g = capture(torch, reuse_step)
+    ms_reuse = replay_ms(torch, g, steps, stream) / steps
     for L in layers:
         L.reuse_weight_quant = False
     out["weight_quant_reuse"] = {"tflops": round(work.flops / (ms_reuse / 1e3) / 1e12, 1),
                                  "ms_per_step": round(ms_reuse, 4),
-                                 "kernels_per_step": 5 * len(layers)}
+                                 "kernels_per_step": 5 * len(layers), "what": "graph replays"}
     # MuonH: every linear's weight gets one optimizer step per iteration
     mw = [(torch.randn((l.N, l.K), device=dev) * 0.02).float() for l in work.linears]
     mg = [torch.randn((l.N, l.K), device=dev) for l in work.linears]
     radii = [float(w.norm()) for w in mw]
 
     def muonh_step():
-        for w, g, r in zip(mw, mg, radii):
-            bfp8.muonh_update(w, g, 0.02, r)
+        for w, g_, r in zip(mw, mg, radii):
+            bfp8.muonh_update(w, g_, 0.02, r)
 
     mu_steps = max(3, min(steps, 20))
     ms_mu = timed(muonh_step, mu_steps)
@@ -652,24 +814,24 @@ def run_reference(args):
     work = workload(args.workload)
     sampler = OracleSample(work)
     per_step = max(0.2, 90.0 / max(1, args.steps + args.warmup))
-    r, dt, _ = sampler.calibrate(per_step)
+    r, _ = sampler.calibrate(per_step)
     for _ in range(args.warmup):
         sampler.run(r)
-    tot_t, tot_f = 0.0, 0
+    tot = {"quant_s": 0.0, "quant_bytes": 0, "gemm_s": 0.0, "flops": 0, "s": 0.0}
     for _ in range(args.steps):
-        dt, fl = sampler.run(r)
-        tot_t += dt
-        tot_f += fl
-    v = tot_f / tot_t / 1e12
+        res = sampler.run(r)
+        for k in tot:
+            tot[k] += res[k]
+    v = tot["flops"] / tot["s"] / 1e12
     line = {
         "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot_t / args.steps, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot["s"] / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
         "config": {"workload": work.name, "passes": "+".join(work.passes),
                    "parallelism": "host cores (OpenMP)", "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": sampler.cores(), "kind": "oracle",
-                         "sample": sampler.describe(r, tot_t / args.steps)},
+                         "sample": sampler.describe(r, tot["s"] / args.steps), **rates(tot)},
         "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

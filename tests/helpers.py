@@ -44,10 +44,14 @@ def gemm_tolerance_ok(y: np.ndarray, y_ref: np.ndarray, rms_ref: float = None):
     return bool(np.all(err <= allow)), ratio
 
 
-def sample_rows(total: int, n: int, seed: int) -> np.ndarray:
-    """n distinct row indices, always including the first and the last row."""
-    if total <= n:
-        return np.arange(total)
+def tile_rows(total: int, seed: int, extra: int = 32, tile: int = TILE) -> np.ndarray:
+    """Row indices that cover every 128-row tile of an output: one random row in each tile
+    (the last, ragged tile included), the first and the last row, and `extra` more random
+    rows. Compared over all columns, they touch every output tile of the GEMM."""
     rng = np.random.default_rng(seed)
-    r = rng.choice(np.arange(1, total - 1), size=n - 2, replace=False)
-    return np.sort(np.concatenate([[0, total - 1], r]))
+    picks = [0, total - 1]
+    for t0 in range(0, total, tile):
+        picks.append(int(rng.integers(t0, min(t0 + tile, total))))
+    if extra:
+        picks += list(rng.integers(0, total, size=extra))
+    return np.unique(np.asarray(picks, dtype=np.int64))

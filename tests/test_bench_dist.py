@@ -70,3 +70,19 @@ def test_reference_arm_line_on_rank_zero():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["value"] > 0 and line["value"] == line["e2e"]["value"]
+
+
+def test_peak_follows_the_sampled_clocks():
+    """Burst peak when the timed region ran at the maximum SM clock with no cap; sustained
+    otherwise (power cap, thermal reasons, or a clock well below its maximum)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6000.0}
+    free = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
+    assert bench.choose_peak(free, peaks, "measured")[:2] == (3600.0, "burst")
+    capped = dict(free, reasons=["sw_power_cap"])
+    assert bench.choose_peak(capped, peaks, "measured")[:2] == (2800.0, "sustained")
+    slow = dict(free, sm_mhz=1500.0)
+    assert bench.choose_peak(slow, peaks, "measured")[:2] == (2800.0, "sustained")
+    unknown = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    assert bench.choose_peak(unknown, peaks, "measured")[1] == "sustained"

@@ -73,6 +73,62 @@ def test_weight_quantisation_is_reused_until_the_weight_changes():
     assert plain.weight_quant_calls == 2
 
 
+def _oracle_step(x, w, dy, M):
+    """y, dx, dW of one step from the oracle's codes and scales of (x, w, dy)."""
+    qx, sx = oracle.quantize_act(x)
+    qw, sw = oracle.quantize_weight(w)
+    qdy, sdy = oracle.quantize_act(dy)
+    qdyt, sdyt = oracle.quantize_transpose(dy)
+    qxt, sxt = oracle.quantize_transpose(x)
+    return (oracle.gemm_fwd(qx, sx, qw, sw), oracle.gemm_dgrad(qdy, sdy, qw, sw),
+            oracle.gemm_wgrad(qdyt, sdyt, qxt, sxt, M), qw, sw)
+
+
+def _check_step(layer, y, dx, dw, x, w, dy, M, what):
+    ry, rdx, rdw, qw, sw = _oracle_step(x, w, dy, M)
+    assert np.array_equal(layer.qw.cpu().numpy(), qw), f"{what}: weight codes"
+    assert np.array_equal(layer.sw.cpu().numpy().view(np.uint32), sw.view(np.uint32)), f"{what}: weight scales"
+    _check(from_dev_bf16(y), ry, f"{what} fwd")
+    _check(from_dev_bf16(dx), rdx, f"{what} dgrad")
+    _check(from_dev_bf16(dw), rdw, f"{what} wgrad")
+
+
+def test_weight_reuse_steps_match_the_oracle():
+    """Micro-batches that reuse W's codes, an optimizer-style in-place update of W (new
+    version: re-quantised), and a change made behind torch's version counter followed by
+    invalidate_weight_quant(): every step's y, dx and dW against the oracle's codes and
+    scales of the weight as it is at that step."""
+    lin, x, w, dy = _case(M=300, K=384, N=256)
+    x2 = wl.random_bits((lin.M, lin.K), 77)
+    dy2 = wl.random_bits((lin.M, lin.N), 78)
+    xd, wd, dyd = to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy)
+    layer = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, reuse_weight_quant=True)
+    # micro-batch 1 quantises W; micro-batch 2 (other x, dy) reuses its codes
+    y = layer.forward(xd, wd).clone()
+    dx, dw = (t.clone() for t in layer.backward(dyd))
+    _check_step(layer, y, dx, dw, x, w, dy, lin.M, "micro-batch 1")
+    y = layer.forward(to_dev_bf16(x2), wd).clone()
+    dx, dw = (t.clone() for t in layer.backward(to_dev_bf16(dy2)))
+    assert layer.weight_quant_calls == 1
+    _check_step(layer, y, dx, dw, x2, w, dy2, lin.M, "micro-batch 2 (reused codes)")
+    # an in-place update of W (what an optimizer step does): new codes and scales
+    step = wl.random_bits((lin.N, lin.K), 79, std=0.01)
+    wd.add_(to_dev_bf16(step))
+    w_new = wd.cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    y = layer.forward(xd, wd).clone()
+    dx, dw = (t.clone() for t in layer.backward(dyd))
+    assert layer.weight_quant_calls == 2
+    _check_step(layer, y, dx, dw, x, w_new, dy, lin.M, "after an in-place update")
+    # a change the version counter does not see, then an explicit invalidation
+    wd.data.mul_(0.75)
+    w_3 = wd.cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    layer.invalidate_weight_quant()
+    y = layer.forward(xd, wd).clone()
+    dx, dw = (t.clone() for t in layer.backward(dyd))
+    assert layer.weight_quant_calls == 3
+    _check_step(layer, y, dx, dw, x, w_3, dy, lin.M, "after invalidation")
+
+
 def test_main_gradient_mode_accumulates_micro_batches():
     lin, x, w, dy = _case(M=257, K=384, N=256)
     xd, wd, dyd = to_dev_bf16(x), to_dev_bf16(w), to_dev_bf16(dy)

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as wl
-from helpers import sample_rows, scales_to_dev, to_dev
+from helpers import scales_to_dev, tile_rows, to_dev
 
 import blockwise_fp8_linear_weight_b300 as bfp8
 
@@ -83,11 +83,11 @@ def test_wgrad_acc_matches_bf16_wgrad_before_rounding():
 
 
 @pytest.mark.parametrize("lin", list(wl.mlp_projections().linears), ids=lambda l: f"{l.name}-M{l.M}")
-def test_wgrad_acc_mlp_shapes_sampled_rows(lin):
+def test_wgrad_acc_mlp_shapes_every_tile(lin):
     x, _, dy = wl.make_linear(lin)
     qdyt, sdyt = oracle.quantize_transpose(dy)
     qxt, sxt = oracle.quantize_transpose(x)
-    rows = sample_rows(lin.N, 32, lin.K)
+    rows = tile_rows(lin.N, lin.K)
     main = np.random.default_rng(5).standard_normal((lin.N, lin.K)).astype(np.float32)
     mg = torch.from_numpy(main).cuda()
     bfp8.fp8_block_gemm_wgrad_acc(to_dev(qdyt), scales_to_dev(sdyt), to_dev(qxt), scales_to_dev(sxt), lin.M, mg)

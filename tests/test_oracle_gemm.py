@@ -206,3 +206,12 @@ def test_wgrad_accumulate_twice_from_zero_doubles(oracle_lib):
     assert np.array_equal(2.0 * once, once + once)
     twice = oracle.gemm_wgrad_accumulate(once.astype(np.float32), qdyt, sdyt, qxt, sxt, 130)
     assert _close(twice, 2.0 * once, rtol=1e-7)
+
+
+@pytest.mark.parametrize("total", [1, 127, 128, 1000, 8192, 32768])
+def test_tile_rows_cover_every_output_tile(total):
+    """The parity tests' row sampler picks at least one row in every 128-row tile."""
+    from helpers import tile_rows
+    r = tile_rows(total, seed=total)
+    assert r.min() == 0 and r.max() == total - 1 and np.all(np.diff(r) > 0)
+    assert set(range((total + 127) // 128)) == set((r // 128).tolist())
