@@ -58,8 +58,6 @@ def parse():
                    help="skip the other workloads (attention, 28-layer stack, single linear, shape sweep)")
     p.add_argument("--gemm-tile-n", type=int, default=0, choices=[0, 128, 192, 256],
                    help="GEMM tile width (0: automatic)")
-    p.add_argument("--gemm-promo-warps", type=int, default=0, choices=[0, 8, 16],
-                   help="GEMM promotion warps per CTA (0: library default)")
     return p.parse_args()
 
 
@@ -454,8 +452,6 @@ def run_ours(args):
     lib_build.build()
     bfp8.load_library()
     bfp8.set_gemm_tile_n(args.gemm_tile_n)
-    if args.gemm_promo_warps:
-        bfp8.set_gemm_promo_warps(args.gemm_promo_warps)
 
     work = workload(args.workload)
     dev = torch.device("cuda", local)

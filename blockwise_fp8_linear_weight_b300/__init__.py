@@ -71,7 +71,6 @@ def load_library(path: str = LIB_PATH):
         "bfp8_set_gemm_tile_n": [c_int],
         "bfp8_set_wait_limit_ns": [i64],
         "bfp8_test_stall_producers": [c_int],
-        "bfp8_set_gemm_promo_warps": [c_int],
         "muonh_partials_len": [ctypes.POINTER(c_int)],
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
         "muonh_apply": [p, i64, p, i64, i64, i64, p, i64, ctypes.c_float, ctypes.c_float, p],
@@ -260,14 +259,6 @@ def set_gemm_tile_n(tile_n: int) -> int:
     rc = load_library().bfp8_set_gemm_tile_n(int(tile_n))
     if rc < 0:
         raise ValueError("tile_n must be 0, 128, 192 or 256")
-    return rc
-
-
-def set_gemm_promo_warps(warps: int) -> int:
-    """Promotion warps per CTA for 256-wide GEMM tiles: 8 or 16. Returns the previous value."""
-    rc = load_library().bfp8_set_gemm_promo_warps(int(warps))
-    if rc < 0:
-        raise ValueError("warps must be 8 or 16")
     return rc
 
 

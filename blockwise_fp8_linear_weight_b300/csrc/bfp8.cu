@@ -30,7 +30,6 @@ constexpr int64_t kMaxGridY = 65535;
 std::atomic<int> g_tile_n{0};
 std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
 std::atomic<int> g_stall{0};
-std::atomic<int> g_promo_warps{8};
 
 // ----------------------------------------------------------------- helpers
 bool aligned(const void* p, uintptr_t a)
@@ -146,7 +145,7 @@ struct GemmProblem {
 template <class Cfg>
 int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int dev)
 {
-    CUtensorMap tmA, tmB, tmSA, tmSB, tmD;
+    CUtensorMap tmA, tmB, tmSA, tmD;
     const int64_t nc = p.gk / 128;
     bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, p.gk, p.gm, p.lda, 128, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -156,14 +155,10 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     else
         ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, p.gk, p.gn, p.ldb, 128, Cfg::BN,
                             CU_TENSOR_MAP_SWIZZLE_128B);
-    // scales: one box holds SGROUP chunks (rows) of 128 (A) or BN (B) scales
+    // A scales: one box holds SGROUP chunks (rows) of 128 scales (B scales are read
+    // by the scale-producer warp with plain loads)
     ok = ok && make_map(&tmSA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sa, p.gm, nc, p.ld_sa * 4, 128, Cfg::SGROUP,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (Cfg::SB_VEC)
-        ok = ok && make_map(&tmSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.sb, p.gn, nc, p.ld_sb * 4, Cfg::BN,
-                            Cfg::SGROUP, CU_TENSOR_MAP_SWIZZLE_NONE);
-    else
-        tmSB = tmSA;  // unused in scalar mode
     if (Cfg::EPI == EPI_F32_ADD)
         ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.d, p.gn, p.gm, p.ldd * 4, 32, 32,
                             CU_TENSOR_MAP_SWIZZLE_128B);
@@ -201,13 +196,15 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     args.sb_scalar = p.sb;
     args.sb_col_stride = p.sb_col_stride;
     args.sb_chunk_stride = p.sb_chunk_stride;
+    args.sb_vec = p.sb;
+    args.ld_sb = p.ld_sb;
     args.status = status;
     args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     args.stall = g_stall.load(std::memory_order_relaxed);
     // persistent grid: one CTA per SM, or one per tile if there are fewer tiles
     const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
     const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
-    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmSB, tmD, args);
+    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmD, args);
     return launch_status();
 }
 
@@ -221,21 +218,21 @@ int dispatch_gemm(const GemmProblem& p, cudaStream_t stream)
     unsigned* status = device_status_ptr(dev);
     if (!status)
         return BFP8_ELAUNCH;
-    if (EPI == EPI_F32_ADD)  // one configuration: 256-wide tiles, 8 promotion warps
+    if constexpr (EPI == EPI_F32_ADD) {  // one configuration: 256-wide tiles, 8 promotion warps
         return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, EPI_F32_ADD>>(p, status, stream, dev);
-    int tn = g_tile_n.load(std::memory_order_relaxed);
-    if (tn == 0)
-        tn = 256;
-    if (tn == 128)
-        return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
-    if constexpr (!B_MN) {
-        // 192-wide tiles: 12 promotion warps of 64 columns (one TMEM load per chunk each)
-        if (tn == 192)
-            return run_gemm<GemmConfig<192, 4, B_MN, SB_VEC, EPI_BF16_TMA, 12>>(p, status, stream, dev);
+    } else {
+        int tn = g_tile_n.load(std::memory_order_relaxed);
+        if (tn == 0)
+            tn = 256;
+        if (tn == 128)
+            return run_gemm<GemmConfig<128, 5, B_MN, SB_VEC>>(p, status, stream, dev);
+        if constexpr (!B_MN) {
+            // 192-wide tiles: 12 promotion warps of 64 columns
+            if (tn == 192)
+                return run_gemm<GemmConfig<192, 4, B_MN, SB_VEC, EPI_BF16_TMA, 12>>(p, status, stream, dev);
+        }
+        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC>>(p, status, stream, dev);
     }
-    if (g_promo_warps.load(std::memory_order_relaxed) == 16)
-        return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC, EPI_BF16_TMA, 16>>(p, status, stream, dev);
-    return run_gemm<GemmConfig<256, 3, B_MN, SB_VEC>>(p, status, stream, dev);
 }
 
 bool gemm_dims_ok(int64_t gm, int64_t gn, int64_t gk)
@@ -674,12 +671,6 @@ extern "C" int bfp8_last_device_status(void* stream)
     return (host & kDevTimeout) ? BFP8_ETIMEOUT : BFP8_OK;
 }
 
-extern "C" int bfp8_set_gemm_promo_warps(int warps)
-{
-    if (warps != 8 && warps != 16)
-        return BFP8_EINVAL;
-    return g_promo_warps.exchange(warps);
-}
 
 extern "C" int bfp8_set_wait_limit_ns(int64_t ns)
 {

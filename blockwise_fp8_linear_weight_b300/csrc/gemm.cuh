@@ -29,11 +29,13 @@
 //               per chunk into one of two TMEM accumulators of BN columns;
 //   warp 2      producer of the scale ring (TMA for the per-row and per-column
 //               scales; plain loads for the scalar B scales);
-//   warps 4..   promotion (8 warps by default; 12 or 16 as options): warp w
-//               owns TMEM lanes 32 (w%4) .. +31 (output rows) and BN/(PW/4)
+//   warps 4..   promotion (8 warps; 12 with 192-wide tiles): warp w owns
+//               TMEM lanes 32 (w%4) .. +31 (output rows) and BN/(PW/4)
 //               columns; per chunk it reads the partial sums with tcgen05.ld
-//               (64 columns per load and wait), releases the TMEM
-//               buffer and accumulates  acc += partial * (sA * sB)  in FP32
+//               in quarters of 32 columns (later quarters loading while earlier
+//               ones are promoted), releases the TMEM buffer once its last
+//               quarter has landed, and accumulates
+//               acc += partial * (sA * sB)  in FP32
 //               registers with packed two-lane FP32 instructions (scalar FP32
 //               instructions issued at this rate halve the tensor core's MMA
 //               rate on sm_103; the packed form leaves it at full speed); after
@@ -47,7 +49,7 @@
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
 // warpgroup to the promotion warpgroups (56/224, or 64/216 with per-column
 // B scales), within the launch budget of 384 x 168 (12 promotion warps at
-// BN = 192: 56/152 within 512 x 128; 16 warps: 32/112 within 640 x 96).
+// BN = 192: 56/152 within 512 x 128).
 // Every mbarrier wait is bounded (mbar_wait); a timeout sets the library's
 // device status word and the kernel unwinds without hanging.
 #pragma once
@@ -83,7 +85,6 @@ struct GemmConfig {
     static constexpr int PROMO_WARPS = PW_;
     static constexpr int GROUPS = PW_ / 4;
     static constexpr int CPW = BN / GROUPS;  // output columns per promotion warp
-    static constexpr int LW = CPW == 64 && PW_ == 16 ? 32 : 64;  // columns per TMEM load
     static constexpr int THREADS = 128 + 32 * PROMO_WARPS;
     static constexpr bool REG_SPLIT = (BN >= 192);
     // TMEM accumulator buffers: as many BN-column buffers as the 512 columns hold
@@ -96,12 +97,21 @@ struct GemmConfig {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SA_BYTES = BM * 4;               // A scales of one chunk
-    static constexpr int SB_BYTES = SB_VEC ? BN * 4 : 0;  // vector-mode B scales of one chunk
+    // Vector-mode B scales of one chunk, stored permuted for the promotion's
+    // 16x256b TMEM layout (thread i holds columns 8g + 2(i%4), +1 of its column
+    // group): per column group h, per lane class q4 = i % 4, the 2G scales of that
+    // class's columns (G = CPW / 8 column pairs), each class padded by 4 floats so
+    // that the four classes' 16-byte reads fall on distinct banks.
+    static constexpr int SBV_G = CPW / 8;
+    static constexpr int SBV_QSTRIDE = 2 * SBV_G + 4;
+    static constexpr int SBV_HSTRIDE = 4 * SBV_QSTRIDE;
+    static constexpr int SBV_CHUNK = GROUPS * SBV_HSTRIDE;  // floats per chunk
+    static constexpr int SB_BYTES = SB_VEC ? SBV_CHUNK * 4 : 0;
     // scalar-mode B scales of one chunk: the 128-column blocks a tile touches (a
     // 192-wide tile at a multiple of 192 touches two)
     static constexpr int SBS_PER_CHUNK = BN == 128 ? 1 : 2;
     static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
-    static constexpr uint32_t SC_TX = SGROUP * (SA_BYTES + SB_BYTES);  // TMA bytes of one scale stage
+    static constexpr uint32_t SC_TX = SGROUP * SA_BYTES;  // TMA bytes of one scale stage (A scales)
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
     // (64 BF16 or 32 FP32 columns; 4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
@@ -124,9 +134,10 @@ struct GemmConfig {
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
     // setmaxnreg split between the producer/MMA warpgroup and the two promotion
     // warpgroups (chosen so that neither side spills on its hot path)
-    static constexpr int REG_LOW = PW_ == 16 ? 32 : (PW_ == 12 ? 56 : (SB_VEC ? 64 : 56));
-    static constexpr int REG_HIGH = PW_ == 16 ? 112 : (PW_ == 12 ? 152 : (SB_VEC ? 216 : 224));
-    static_assert(PW_ == 8 || PW_ == 12 || PW_ == 16, "8, 12 or 16 promotion warps");
+    static constexpr int REG_LOW = PW_ == 12 ? 56 : 56;
+    static constexpr int REG_HIGH = PW_ == 12 ? 152 : 224;
+    static_assert(PW_ == 8 || PW_ == 12, "8 or 12 promotion warps");
+    static_assert(CPW % 64 == 0, "promotion works on pairs of 32-column quarters");
     static_assert(!REG_SPLIT || 128 * REG_LOW + 32 * PW_ * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
 };
 
@@ -136,6 +147,8 @@ struct GemmArgs {
     int n_fastest;            // tile order: 1 = sweep the N tiles of a row block first
     const float* sb_scalar;   // scalar mode: sB(c, j) = sb_scalar[(j/128) * sb_col_stride + c * sb_chunk_stride]
     int64_t sb_col_stride, sb_chunk_stride;
+    const float* sb_vec;      // vector mode: sB(c, j) = sb_vec[c * ld_sb + j]
+    int64_t ld_sb;
     unsigned* status;
     unsigned long long wait_ns;  // limit of one mbarrier wait
     int stall;                   // test switch: the operand producer issues no copies
@@ -162,8 +175,8 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& args, int t, int& m0
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     bfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                     const __grid_constant__ CUtensorMap tmD, const GemmArgs args)
+                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
+                     const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -215,8 +228,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
-        if (Cfg::SB_VEC)
-            tma_prefetch_desc(&tmSB);
         tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
@@ -294,7 +305,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ok = false;
                     break;
                 }
-                if (!Cfg::SB_VEC) {
+                if constexpr (Cfg::SB_VEC) {
+                    // the group's per-column scales, a column pair per lane and step,
+                    // written in the promotion's permuted layout (zero past the edges)
+                    float* dst = sSB + qs * Cfg::SGROUP * Cfg::SBV_CHUNK;
+                    constexpr int PAIRS = Cfg::BN / 2;
+#pragma unroll 4
+                    for (int u = lane; u < Cfg::SGROUP * PAIRS; u += 32) {
+                        const int cc = u / PAIRS, n = 2 * (u % PAIRS);
+                        const int c = c0 + cc;
+                        float2 v = make_float2(0.0f, 0.0f);
+                        if (c < nc && n0 + n < args.gn)
+                            v = __ldg(reinterpret_cast<const float2*>(args.sb_vec + static_cast<int64_t>(c) * args.ld_sb +
+                                                                      n0 + n));
+                        const int h = n / Cfg::CPW, w = n % Cfg::CPW;
+                        *reinterpret_cast<float2*>(dst + cc * Cfg::SBV_CHUNK + h * Cfg::SBV_HSTRIDE +
+                                                   ((w & 7) >> 1) * Cfg::SBV_QSTRIDE + 2 * (w >> 3)) = v;
+                    }
+                    __syncwarp();  // the stores above happen before lane 0's arrive (release)
+                } else {
                     // lane i: chunk c0 + i / SBS_PER_CHUNK, the tile's 128-column block i % SBS_PER_CHUNK
                     if (lane < NSBS) {
                         const int c = c0 + lane / Cfg::SBS_PER_CHUNK;
@@ -310,8 +339,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&sfull[qs], Cfg::SC_TX);
                     tma_load_2d(sSA + qs * Cfg::SGROUP * Cfg::BM, &tmSA, &sfull[qs], m0, c0);
-                    if (Cfg::SB_VEC)
-                        tma_load_2d(sSB + qs * Cfg::SGROUP * Cfg::BN, &tmSB, &sfull[qs], n0, c0);
                 }
                 ++issued;
             }
@@ -408,41 +435,103 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 break;
             tc_fence_after_sync();
             const int slot = qs * Cfg::SGROUP + gi;  // this chunk's row of the scale stage
-            const float sa = sSA[slot * Cfg::BM + row];
-            const float sb_c =
-                Cfg::SB_VEC ? 0.0f
-                            : sSBs[slot * Cfg::SBS_PER_CHUNK + ((n0 + half * CPW) >> 7) - (n0 >> 7)];
-            const uint64_t sa2 = pack_f32x2(sa, sa);
-            const float sc = sa * sb_c;
-            const uint64_t sc2 = pack_f32x2(sc, sc);
             const uint32_t t_base =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * Cfg::BUF_STRIDE + half * CPW;
-            constexpr int LW = Cfg::LW;
+            auto release = [&]() {  // to the MMA issuer
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&tempty[b]);
+            };
+            uint32_t ra[32], rb[32];
+            if constexpr (Cfg::SB_VEC) {
+                // Per-column B scales. TMEM is read in the 16x256b layout: a load of the
+                // warp's lanes 0-15 (ra) or 16-31 (rb) over 64 columns gives thread i
+                // the rows i/4 and i/4 + 8 of those lanes and, for each 8-column step,
+                // the column pair 2(i%4), +1; so the thread's 128 values are 4 rows x 16
+                // column pairs, and it needs the scales of 32 columns, not 128. Both
+                // lane halves use the same columns: one 16-byte read serves 16 values.
+                constexpr int G = Cfg::SBV_G;
+                constexpr int NB = CPW / 64;
+                static_assert(NB == 1 || NB == 2, "one or two 64-column blocks per warp");
+                uint64_t sa2[4];
 #pragma unroll
-            for (int j = 0; j < CPW / LW; ++j) {
-                uint64_t p[LW / 2];  // columns j*LW .. j*LW+LW-1 of the partial sums, as pairs
-                tmem_ld_pairs<LW>(t_base + j * LW, p);
-                if (j == CPW / LW - 1) {
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&tempty[b]);
+                for (int k = 0; k < 4; ++k) {
+                    const float v = sSA[slot * Cfg::BM + quarter * 32 + (lane >> 2) + 8 * k];
+                    sa2[k] = pack_f32x2(v, v);
                 }
-                uint64_t* a = acc + j * (LW / 2);
-                if (Cfg::SB_VEC) {
-                    // per-column scales: broadcast 16-byte shared-memory reads (two column pairs each)
-                    const ulonglong2* sbv =
-                        reinterpret_cast<const ulonglong2*>(sSB + slot * Cfg::BN + half * CPW + j * LW);
+                const float* sbq = sSB + slot * Cfg::SBV_CHUNK + half * Cfg::SBV_HSTRIDE + (lane & 3) * Cfg::SBV_QSTRIDE;
+                auto promote_block = [&](const uint32_t(&lo)[32], const uint32_t(&hi)[32], int j) {
+                    const ulonglong2* v2 = reinterpret_cast<const ulonglong2*>(sbq + 16 * j);
 #pragma unroll
-                    for (int i = 0; i < LW / 4; ++i) {
-                        const ulonglong2 v = sbv[i];
-                        ffma2(a[2 * i], fmul2(p[2 * i], v.x), sa2);
-                        ffma2(a[2 * i + 1], fmul2(p[2 * i + 1], v.y), sa2);
+                    for (int t2 = 0; t2 < 4; ++t2) {
+                        const ulonglong2 v = v2[t2];  // scales of pairs 8j + 2t2 (x) and 8j + 2t2 + 1 (y)
+                        const int gp = 8 * j + 2 * t2;
+                        const int r0 = 8 * t2;        // registers of the 8-column steps 2t2 and 2t2 + 1
+                        ffma2(acc[0 * G + gp], fmul2(pair(lo[r0], lo[r0 + 1]), v.x), sa2[0]);
+                        ffma2(acc[1 * G + gp], fmul2(pair(lo[r0 + 2], lo[r0 + 3]), v.x), sa2[1]);
+                        ffma2(acc[0 * G + gp + 1], fmul2(pair(lo[r0 + 4], lo[r0 + 5]), v.y), sa2[0]);
+                        ffma2(acc[1 * G + gp + 1], fmul2(pair(lo[r0 + 6], lo[r0 + 7]), v.y), sa2[1]);
+                        ffma2(acc[2 * G + gp], fmul2(pair(hi[r0], hi[r0 + 1]), v.x), sa2[2]);
+                        ffma2(acc[3 * G + gp], fmul2(pair(hi[r0 + 2], hi[r0 + 3]), v.x), sa2[3]);
+                        ffma2(acc[2 * G + gp + 1], fmul2(pair(hi[r0 + 4], hi[r0 + 5]), v.y), sa2[2]);
+                        ffma2(acc[3 * G + gp + 1], fmul2(pair(hi[r0 + 6], hi[r0 + 7]), v.y), sa2[3]);
                     }
+                };
+                const uint32_t t_hi = t_base + (16u << 16);
+                tmem_ld16x256_start(t_base, ra);
+                tmem_ld16x256_start(t_hi, rb);
+                tmem_ld_wait(ra);
+                tmem_ld_wait(rb);
+                if constexpr (NB == 1) {
+                    release();
+                    promote_block(ra, rb, 0);
                 } else {
+                    promote_block(ra, rb, 0);
+                    tmem_ld16x256_start(t_base + 64, ra);
+                    tmem_ld16x256_start(t_hi + 64, rb);
+                    tmem_ld_wait(ra);
+                    tmem_ld_wait(rb);
+                    release();
+                    promote_block(ra, rb, 1);
+                }
+            } else {
+                // Scalar B scales (one per 128-column block): the 32x32b layout, thread =
+                // row, one scale product per chunk. The warp's CPW columns go in quarters
+                // of 32 through two register buffers. The first two quarters are loaded
+                // together; each later one is loaded into the buffer just promoted, while
+                // the other buffer is promoted. The TMEM buffer goes back to the MMA
+                // issuer as soon as its last quarter has landed in registers.
+                constexpr int NQ = CPW / 32;
+                static_assert(NQ == 2 || NQ == 4, "two or four quarters per warp");
+                const float sa = sSA[slot * Cfg::BM + row];
+                const float sb_c = sSBs[slot * Cfg::SBS_PER_CHUNK + ((n0 + half * CPW) >> 7) - (n0 >> 7)];
+                const float sc = sa * sb_c;
+                const uint64_t sc2 = pack_f32x2(sc, sc);
+                auto promote = [&](const uint32_t(&r)[32], int j) {
+                    uint64_t* a = acc + j * 16;
 #pragma unroll
-                    for (int i = 0; i < LW / 2; ++i)
-                        ffma2(a[i], p[i], sc2);
+                    for (int i = 0; i < 16; ++i)
+                        ffma2(a[i], pair(r[2 * i], r[2 * i + 1]), sc2);
+                };
+                tmem_ld32_start(t_base, ra);
+                tmem_ld32_start(t_base + 32, rb);
+                tmem_ld_wait(ra);
+                tmem_ld_wait(rb);
+                if constexpr (NQ == 2) {
+                    release();
+                    promote(ra, 0);
+                    promote(rb, 1);
+                } else {
+                    promote(ra, 0);
+                    tmem_ld32_start(t_base + 64, ra);
+                    promote(rb, 1);
+                    tmem_ld32_start(t_base + 96, rb);
+                    tmem_ld_wait(ra);
+                    tmem_ld_wait(rb);
+                    release();
+                    promote(ra, 2);
+                    promote(rb, 3);
                 }
             }
             // the group's last chunk (or the tile's): this warp is done with the stage
@@ -464,24 +553,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const int col0 = n0 + half * CPW;
                 if constexpr (Cfg::EPI == EPI_F32_ADD) {
                     // FP32 boxes of 32 columns: the slab holds CPW/64 of them, so the
-                    // CPW/32 boxes of the row go out in two rounds
+                    // CPW/32 boxes of the row go out in two rounds. The accumulators are
+                    // in the 16x256b layout (4 rows x G column pairs per thread): each pair
+                    // goes to its row and column of a 128-byte-swizzled box.
+                    static_assert(Cfg::SB_VEC, "the FP32 accumulate epilogue serves the weight gradient");
                     constexpr int SLAB = CPW / 64;
+                    constexpr int G = Cfg::SBV_G;
+                    const int q4 = lane & 3, rs = lane >> 2;
 #pragma unroll
                     for (int round = 0; round < 2; ++round) {
                         if (lane == 0)
                             tma_store_wait_read_all();  // earlier adds have read the slab
                         __syncwarp();
 #pragma unroll
-                        for (int bx = 0; bx < SLAB; ++bx) {
-                            uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
-                            const uint64_t* v = acc + (round * SLAB + bx) * 16;
+                        for (int k = 0; k < 4; ++k) {
+                            const int r = rs + 8 * k;
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const uint4 pk = make_uint4(static_cast<uint32_t>(v[2 * k]),
-                                                            static_cast<uint32_t>(v[2 * k] >> 32),
-                                                            static_cast<uint32_t>(v[2 * k + 1]),
-                                                            static_cast<uint32_t>(v[2 * k + 1] >> 32));
-                                *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                            for (int gg = 0; gg < SLAB * 4; ++gg) {
+                                const int chunk16 = 2 * (gg & 3) + (q4 >> 1);
+                                *reinterpret_cast<uint64_t*>(my_out + (gg >> 2) * Cfg::BOX_BYTES + r * 128 +
+                                                             ((chunk16 ^ (r & 7)) << 4) + 8 * (q4 & 1)) =
+                                    acc[k * G + round * SLAB * 4 + gg];
                             }
                         }
                         fence_proxy_async_smem();
@@ -500,18 +592,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (lane == 0)
                         tma_store_wait_read_all();  // this warp's previous stores have left the slab
                     __syncwarp();
+                    if constexpr (Cfg::SB_VEC) {
+                        // 16x256b layout: each BF16 pair goes to its row and column of a
+                        // 128-byte-swizzled 32 x 64 box
+                        constexpr int G = Cfg::SBV_G;
+                        const int q4 = lane & 3, rs = lane >> 2;
 #pragma unroll
-                    for (int bx = 0; bx < CPW / 64; ++bx) {
-                        uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
+                        for (int k = 0; k < 4; ++k) {
+                            const int r = rs + 8 * k;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const uint64_t* v = acc + bx * 32 + k * 4;
-                            uint4 pk;
-                            pk.x = cvt_bf16x2(v[0]);
-                            pk.y = cvt_bf16x2(v[1]);
-                            pk.z = cvt_bf16x2(v[2]);
-                            pk.w = cvt_bf16x2(v[3]);
-                            *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                            for (int gp = 0; gp < G; ++gp)
+                                *reinterpret_cast<uint32_t*>(my_out + (gp >> 3) * Cfg::BOX_BYTES + r * 128 +
+                                                             (((gp & 7) ^ (r & 7)) << 4) + 4 * q4) =
+                                    cvt_bf16x2(acc[k * G + gp]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int bx = 0; bx < CPW / 64; ++bx) {
+                            uint8_t* box = my_out + bx * Cfg::BOX_BYTES;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const uint64_t* v = acc + bx * 32 + k * 4;
+                                uint4 pk;
+                                pk.x = cvt_bf16x2(v[0]);
+                                pk.y = cvt_bf16x2(v[1]);
+                                pk.z = cvt_bf16x2(v[2]);
+                                pk.w = cvt_bf16x2(v[3]);
+                                *reinterpret_cast<uint4*>(box + lane * 128 + ((k ^ (lane & 7)) * 16)) = pk;
+                            }
                         }
                     }
                     fence_proxy_async_smem();

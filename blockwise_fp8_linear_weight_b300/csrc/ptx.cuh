@@ -217,64 +217,48 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar)
                  : "memory");
 }
 
-// 32 lanes x 64 consecutive 32-bit columns starting at taddr, waited for, and
-// returned as 32 packed pairs of neighbouring columns (column 2i in the low
-// word of p[i]). Loading, waiting and pairing in one block lets the register
-// allocator place each pair in a 64-bit register directly, so the packed FP32
-// instructions that consume them need no register moves.
-__device__ __forceinline__ void tmem_ld_x64_pairs(uint32_t taddr, uint64_t (&p)[32])
+// Starts loading 32 lanes x 32 consecutive 32-bit TMEM columns at taddr into r
+// (column i in r[i]). The registers are written asynchronously: they may be read
+// only after tmem_ld_wait(r), which names them as operands, so that the compiler
+// keeps every use of r after the wait and no other value in r's registers.
+__device__ __forceinline__ void tmem_ld32_start(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile(
-        "{\n\t.reg .b32 r<64>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, "
-        "r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31, "
-        "r32, r33, r34, r35, r36, r37, r38, r39, r40, r41, r42, r43, r44, r45, r46, r47, "
-        "r48, r49, r50, r51, r52, r53, r54, r55, r56, r57, r58, r59, r60, r61, r62, r63}, [%32];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
-        "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t"
-        "mov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
-        "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\t"
-        "mov.b64 %16, {r32, r33};\n\tmov.b64 %17, {r34, r35};\n\tmov.b64 %18, {r36, r37};\n\tmov.b64 %19, {r38, r39};\n\t"
-        "mov.b64 %20, {r40, r41};\n\tmov.b64 %21, {r42, r43};\n\tmov.b64 %22, {r44, r45};\n\tmov.b64 %23, {r46, r47};\n\t"
-        "mov.b64 %24, {r48, r49};\n\tmov.b64 %25, {r50, r51};\n\tmov.b64 %26, {r52, r53};\n\tmov.b64 %27, {r54, r55};\n\t"
-        "mov.b64 %28, {r56, r57};\n\tmov.b64 %29, {r58, r59};\n\tmov.b64 %30, {r60, r61};\n\tmov.b64 %31, {r62, r63};\n\t}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]),
-          "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15]),
-          "=l"(p[16]), "=l"(p[17]), "=l"(p[18]), "=l"(p[19]), "=l"(p[20]), "=l"(p[21]), "=l"(p[22]), "=l"(p[23]),
-          "=l"(p[24]), "=l"(p[25]), "=l"(p[26]), "=l"(p[27]), "=l"(p[28]), "=l"(p[29]), "=l"(p[30]), "=l"(p[31])
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
 }
 
-// As tmem_ld_x64_pairs for 32 columns (16 pairs).
-__device__ __forceinline__ void tmem_ld_x32_pairs(uint32_t taddr, uint64_t (&p)[16])
+// Starts loading lanes L..L+15 (L = the address's lane field) x 64 TMEM columns
+// in the 16x256b layout: for each 8-column step s (0..7), thread i receives
+// r[4s], r[4s+1] = columns 8s + 2(i%4), +1 of lane L + i/4, and r[4s+2], r[4s+3]
+// = the same columns of lane L + i/4 + 8. Complete with tmem_ld_wait(r).
+__device__ __forceinline__ void tmem_ld16x256_start(uint32_t taddr, uint32_t (&r)[32])
 {
     asm volatile(
-        "{\n\t.reg .b32 r<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, "
-        "r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
-        "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t"
-        "mov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
-        "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\t}"
-        : "=l"(p[0]), "=l"(p[1]), "=l"(p[2]), "=l"(p[3]), "=l"(p[4]), "=l"(p[5]), "=l"(p[6]), "=l"(p[7]),
-          "=l"(p[8]), "=l"(p[9]), "=l"(p[10]), "=l"(p[11]), "=l"(p[12]), "=l"(p[13]), "=l"(p[14]), "=l"(p[15])
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
 }
 
-template <int NCOLS>
-__device__ __forceinline__ void tmem_ld_pairs(uint32_t taddr, uint64_t (&p)[NCOLS / 2])
+// Waits for every TMEM load this thread started; r (the registers of the last
+// load) is named read-write so that no use of r moves above the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 {
-    static_assert(NCOLS == 32 || NCOLS == 64, "32 or 64 columns");
-    if constexpr (NCOLS == 64)
-        tmem_ld_x64_pairs(taddr, p);
-    else
-        tmem_ld_x32_pairs(taddr, p);
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// {lo, hi} as one packed pair
+__device__ __forceinline__ uint64_t pair(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
 }
 
 // d = a * s on packed pairs

@@ -211,11 +211,6 @@ int bfp8_test_stall_producers(int on);
  * every thread. */
 int bfp8_set_gemm_tile_n(int tile_n);
 
-/* Tuning knob for the 256-wide GEMM tiles: promotion warps per CTA, 8
- * (default; 128 columns each) or 16 (64 columns each, more latency hiding,
- * fewer registers per thread). Returns the previous setting, or BFP8_EINVAL.
- * Applies to later calls from every thread. */
-int bfp8_set_gemm_promo_warps(int warps);
 
 #ifdef __cplusplus
 }

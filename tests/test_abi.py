@@ -25,7 +25,7 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
-                          "bfp8_set_gemm_promo_warps", "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers",
+                          "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers",
                           "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
@@ -42,9 +42,6 @@ def test_tile_knob(lib):
     assert lib.bfp8_set_gemm_tile_n(64) == EINVAL
     prev = lib.bfp8_set_gemm_tile_n(256)
     assert lib.bfp8_set_gemm_tile_n(prev) == 256
-    assert lib.bfp8_set_gemm_promo_warps(12) == EINVAL
-    prev = lib.bfp8_set_gemm_promo_warps(16)
-    assert lib.bfp8_set_gemm_promo_warps(prev) == 16
 
 
 def test_wait_limit_and_stall_switch_arguments(lib):

@@ -24,18 +24,14 @@ pytestmark = pytest.mark.gpu
 TILE = 128
 
 
-@pytest.fixture(params=[(128, 8), (192, 8), (256, 8), (256, 16)],
-                ids=lambda p: f"tileN{p[0]}-warps{p[1]}")
+@pytest.fixture(params=[128, 192, 256], ids=lambda t: f"tileN{t}")
 def tile_n(request):
     """Every tile configuration: 128-wide tiles, 192-wide tiles with 12 promotion warps
-    (forward and weight gradient; the input gradient then runs 256-wide), 256-wide
-    tiles, and 256-wide tiles with 16 promotion warps."""
-    tn, pw = request.param
-    prev_t = bfp8.set_gemm_tile_n(tn)
-    prev_w = bfp8.set_gemm_promo_warps(pw)
-    yield tn
+    (forward and weight gradient; the input gradient then runs 256-wide), and 256-wide
+    tiles (the default)."""
+    prev_t = bfp8.set_gemm_tile_n(request.param)
+    yield request.param
     bfp8.set_gemm_tile_n(prev_t)
-    bfp8.set_gemm_promo_warps(prev_w)
 
 
 def _check(y_gpu, y_ref, what):
