@@ -17,6 +17,8 @@ Entry points (same names as the C ABI):
   fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad): main_grad [N, K] f32 += dW
 MuonH (one optimizer step for one weight matrix):
   muonh_update(w, g, lr, radius)  # w FP32 in place; see muonh_update's docstring
+  bf16_gemm_axpby(a, b, c, alpha, beta) -> d = alpha a b + beta c (BF16, FP32 sums)
+  muonh_newton_schulz(x)          # Newton-Schulz iterations on a BF16 matrix, in place
 Scale tensors are allocated with a row stride rounded up to 4 elements so that
 the GEMMs' TMA loads see 16-byte rows; the returned tensors are views of the
 valid columns.
@@ -75,6 +77,9 @@ def load_library(path: str = LIB_PATH):
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
         "muonh_apply": [p, i64, p, i64, i64, i64, p, i64, ctypes.c_float, ctypes.c_float, p],
         "muonh_apply_static": [p, i64, p, i64, i64, i64, ctypes.c_float, ctypes.c_float, p],
+        "bf16_gemm_axpby": [p, i64, p, i64, c_int, p, i64, p, i64, i64, i64, i64, ctypes.c_float, ctypes.c_float, p],
+        "muonh_newton_schulz_work_bytes": [i64, i64, ctypes.POINTER(i64)],
+        "muonh_newton_schulz": [p, i64, i64, i64, p, i64, c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float, p],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -398,27 +403,50 @@ def muonh_apply_static(w, u, lr: float, radius: float):
     return w
 
 
-def newton_schulz_bf16(x, steps: int = 5, coeffs=MUON_NS_COEFFS):
-    """Quintic Newton-Schulz iterations X <- a X + (b A + c A^2) X, A = X X^T, on the
-    orientation with fewer rows; plain BF16 GEMMs with FP32 accumulation (cuBLAS)."""
+def bf16_gemm_axpby(a, b, c=None, alpha: float = 1.0, beta: float = 0.0, b_mn_major: bool = False, d=None):
+    """d = bf16(alpha * a @ B + beta * c) with a [M, K] and B = b^T (b [N, K]) or B = b (b [K, N],
+    b_mn_major=True), all BF16; the products are summed in FP32 by the library's tcgen05 kernel."""
+    lib = load_library()
+    _req(a, torch.bfloat16, "a")
+    _req(b, torch.bfloat16, "b")
+    M, K = a.shape
+    N = b.shape[1] if b_mn_major else b.shape[0]
+    d = torch.empty((M, N), dtype=torch.bfloat16, device=a.device) if d is None else d
+    if c is not None:
+        _req(c, torch.bfloat16, "c")
+    _check("bf16_gemm_axpby", lib.bf16_gemm_axpby(
+        _ptr(a), a.stride(0), _ptr(b), b.stride(0), 1 if b_mn_major else 0,
+        _ptr(c) if c is not None else None, c.stride(0) if c is not None else 0,
+        _ptr(d), d.stride(0), M, N, K, float(alpha), float(beta), _stream()))
+    return d
+
+
+def muonh_newton_schulz(x, steps: int = 5, coeffs=MUON_NS_COEFFS, work=None):
+    """Quintic Newton-Schulz iterations X <- a X + (b A + c A^2) X, A = X X^T, on the orientation
+    with fewer rows, in place on a BF16 matrix x (rows, cols multiples of 8). Every product runs in
+    the library's BF16 tcgen05 GEMM; work is a caller buffer of muonh_newton_schulz_work_bytes."""
+    lib = load_library()
+    _req(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    if work is None:
+        n = ctypes.c_int64(0)
+        _check("muonh_newton_schulz_work_bytes", lib.muonh_newton_schulz_work_bytes(rows, cols, ctypes.byref(n)))
+        work = torch.empty(n.value, dtype=torch.uint8, device=x.device)
     a, b, c = coeffs
-    t = x.shape[0] > x.shape[1]
-    if t:
-        x = x.t()
-    for _ in range(steps):
-        A = x @ x.t()
-        B = torch.addmm(A, A, A, beta=b, alpha=c)
-        x = torch.addmm(x, B, x, beta=a, alpha=1.0)
-    return x.t() if t else x
+    _check("muonh_newton_schulz", lib.muonh_newton_schulz(
+        _ptr(x), rows, cols, x.stride(0), _ptr(work), work.numel(), int(steps), float(a), float(b), float(c),
+        _stream()))
+    return x
 
 
 def muonh_update(w, g, lr: float, radius: float, steps: int = 5, coeffs=MUON_NS_COEFFS, eps: float = 1e-7):
     """One MuonH step for one weight matrix, in place: w (FP32 [N, K]) moves by a relative
     step lr along the orthogonalised gradient and is projected back to |w|_F = radius.
 
-    X0 = g / (|g| + eps) (library kernel), U = Newton-Schulz(X0) (BF16 GEMMs),
-    w = radius (w - lr radius U/|U|) / |w - lr radius U/|U|| (library kernels)."""
+    Three library calls: X0 = g / (|g| + eps) (muonh_normalize), U = Newton-Schulz(X0) in
+    place (muonh_newton_schulz), w = radius (w - lr radius U/|U|) / |w - lr radius U/|U||
+    (muonh_apply)."""
     partials = _muonh_partials(w.device)
     x = muonh_normalize(g, eps=eps, partials=partials)
-    u = newton_schulz_bf16(x, steps, coeffs).contiguous()
-    return muonh_apply(w, u, lr, radius, partials=partials)
+    muonh_newton_schulz(x, steps, coeffs)
+    return muonh_apply(w, x, lr, radius, partials=partials)

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "bf16_gemm.cuh"
 #include "bfp8.h"
 #include "gemm.cuh"
 #include "muonh.cuh"
@@ -694,4 +695,165 @@ extern "C" int bfp8_set_gemm_tile_n(int tile_n)
     if (tile_n != 0 && tile_n != 128 && tile_n != 192 && tile_n != 256)
         return BFP8_EINVAL;
     return g_tile_n.exchange(tile_n);
+}
+
+// =================================================================== BF16 GEMM (Newton-Schulz)
+namespace bfp8 {
+namespace {
+
+template <bool B_MN>
+int run_bf16_gemm(const void* a, int64_t lda, const void* b, int64_t ldb, const void* c, int64_t ldc, void* d,
+                  int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha, float beta, cudaStream_t stream, int dev,
+                  unsigned* status)
+{
+    using Cfg = Bf16GemmConfig<B_MN>;
+    CUtensorMap tmA, tmB, tmD;
+    bool ok = make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, K, M, lda * 2, Cfg::BK, Cfg::BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (B_MN)
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b, N, K, ldb * 2, 64, Cfg::BK,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && make_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b, K, N, ldb * 2, Cfg::BK, Cfg::BN,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, N, M, ldd * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok)
+        return BFP8_ELAUNCH;
+    static std::atomic<bool> attr_set[kMaxDevices];
+    auto kern = bf16_gemm_kernel<Cfg>;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    Bf16GemmArgs args;
+    args.gm = static_cast<int>(M);
+    args.gn = static_cast<int>(N);
+    args.gk = static_cast<int>(K);
+    args.tiles_m = static_cast<int>((M + Cfg::BM - 1) / Cfg::BM);
+    args.tiles_n = static_cast<int>((N + Cfg::BN - 1) / Cfg::BN);
+    args.kblocks = static_cast<int>((K + Cfg::BK - 1) / Cfg::BK);
+    args.alpha = alpha;
+    args.beta = beta;
+    args.c = beta != 0.0f ? static_cast<const uint16_t*>(c) : nullptr;
+    args.ldc = ldc;
+    args.status = status;
+    args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    args.stall = g_stall.load(std::memory_order_relaxed);
+    const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
+    const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
+    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, args);
+    return launch_status();
+}
+
+int bf16_gemm_checked(const void* a, int64_t lda, const void* b, int64_t ldb, int b_mn_major, const void* c,
+                      int64_t ldc, void* d, int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                      cudaStream_t stream)
+{
+    if (M < 1 || N < 1 || K < 1 || (b_mn_major != 0 && b_mn_major != 1))
+        return BFP8_EINVAL;
+    if (N % 8 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return BFP8_ESHAPE;
+    if (!a || !b || !d || (beta != 0.0f && !c) || !(alpha == alpha) || !(beta == beta))
+        return BFP8_EINVAL;
+    if (lda < K || ldb < (b_mn_major ? N : K) || ldd < N || (beta != 0.0f && ldc < N))
+        return BFP8_EINVAL;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(d, 16) || (beta != 0.0f && !aligned(c, 16)) || lda % 8 ||
+        ldb % 8 || ldd % 8 || (beta != 0.0f && ldc % 8))
+        return BFP8_EALIGN;
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    unsigned* status = device_status_ptr(dev);
+    if (!status)
+        return BFP8_ELAUNCH;
+    if (b_mn_major)
+        return run_bf16_gemm<true>(a, lda, b, ldb, c, ldc, d, ldd, M, N, K, alpha, beta, stream, dev, status);
+    return run_bf16_gemm<false>(a, lda, b, ldb, c, ldc, d, ldd, M, N, K, alpha, beta, stream, dev, status);
+}
+
+int64_t round8(int64_t x)
+{
+    return (x + 7) / 8 * 8;
+}
+
+// Workspace of muonh_newton_schulz: A and B [r][r8], Y0 and Y1 [r][c8] (BF16),
+// r = min(rows, cols), c = max(rows, cols), row strides rounded up to 8 elements.
+int64_t ns_work_bytes(int64_t rows, int64_t cols)
+{
+    const int64_t r = std::min(rows, cols), c = std::max(rows, cols);
+    return 2 * (2 * r * round8(r) + 2 * r * round8(c));
+}
+
+}  // namespace
+}  // namespace bfp8
+
+extern "C" int bf16_gemm_axpby(const void* a, int64_t lda, const void* b, int64_t ldb, int b_mn_major, const void* c,
+                               int64_t ldc, void* d, int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha,
+                               float beta, void* stream)
+{
+    return bf16_gemm_checked(a, lda, b, ldb, b_mn_major, c, ldc, d, ldd, M, N, K, alpha, beta,
+                             static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int muonh_newton_schulz_work_bytes(int64_t rows, int64_t cols, int64_t* bytes)
+{
+    if (!bytes || rows < 1 || cols < 1)
+        return BFP8_EINVAL;
+    *bytes = ns_work_bytes(rows, cols);
+    return BFP8_OK;
+}
+
+extern "C" int muonh_newton_schulz(void* x, int64_t rows, int64_t cols, int64_t ldx, void* work, int64_t work_bytes,
+                                   int steps, float a, float b, float c, void* stream)
+{
+    if (rows < 1 || cols < 1 || steps < 0 || !x || !work || ldx < cols)
+        return BFP8_EINVAL;
+    if (rows % 8 || cols % 8 || rows > kMaxDim || cols > kMaxDim || (rows + 31) / 32 > kMaxGridY)
+        return BFP8_ESHAPE;
+    if (work_bytes < ns_work_bytes(rows, cols))
+        return BFP8_EINVAL;
+    if (!aligned(x, 16) || ldx % 8 || !aligned(work, 16))
+        return BFP8_EALIGN;
+    int rc = check_arch(nullptr);
+    if (rc != BFP8_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tr = rows > cols;  // iterate on the orientation with fewer rows
+    const int64_t r = tr ? cols : rows, cc = tr ? rows : cols;
+    const int64_t ldr = round8(r), ldc = round8(cc);
+    uint16_t* A = static_cast<uint16_t*>(work);
+    uint16_t* B = A + r * ldr;
+    uint16_t* Y[2] = {B + r * ldr, B + r * ldr + r * ldc};
+    uint16_t* xs = static_cast<uint16_t*>(x);
+    const dim3 blk(32, 8);
+    const dim3 grid_in(static_cast<unsigned>((cols + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
+    if (tr)
+        bf16_copy_kernel<true><<<grid_in, blk, 0, st>>>(xs, rows, cols, ldx, Y[0], ldc);
+    else
+        bf16_copy_kernel<false><<<grid_in, blk, 0, st>>>(xs, rows, cols, ldx, Y[0], ldc);
+    if ((rc = launch_status()) != BFP8_OK)
+        return rc;
+    int cur = 0;
+    for (int i = 0; i < steps; ++i) {
+        const uint16_t* y = Y[cur];
+        // A = Y Y^T (contraction over the long side)
+        rc = bf16_gemm_checked(y, ldc, y, ldc, 0, nullptr, 0, A, ldr, r, r, cc, 1.0f, 0.0f, st);
+        // B = b A + c A A (A read as [K][N] for the second factor)
+        if (rc == BFP8_OK)
+            rc = bf16_gemm_checked(A, ldr, A, ldr, 1, A, ldr, B, ldr, r, r, r, c, b, st);
+        // Y' = a Y + B Y (Y read as [K][N])
+        if (rc == BFP8_OK)
+            rc = bf16_gemm_checked(B, ldr, y, ldc, 1, y, ldc, Y[cur ^ 1], ldc, r, cc, r, 1.0f, a, st);
+        if (rc != BFP8_OK)
+            return rc;
+        cur ^= 1;
+    }
+    const dim3 grid_out(static_cast<unsigned>((cc + 31) / 32), static_cast<unsigned>((r + 31) / 32));
+    if (tr)
+        bf16_copy_kernel<true><<<grid_out, blk, 0, st>>>(Y[cur], r, cc, ldc, xs, ldx);
+    else
+        bf16_copy_kernel<false><<<grid_out, blk, 0, st>>>(Y[cur], r, cc, ldc, xs, ldx);
+    return launch_status();
 }

@@ -239,4 +239,31 @@ __global__ void __launch_bounds__(kMuonThreads) muonh_apply_kernel(float* __rest
     }
 }
 
+// dst[j][i] = src[i][j] for BF16 src [rows][cols] (transpose), or dst[i][j] = src[i][j]
+// (copy), through 32 x 32 shared-memory tiles. grid (ceil(cols/32), ceil(rows/32)), 32 x 8.
+template <bool TRANSPOSE>
+__global__ void __launch_bounds__(256) bf16_copy_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
+                                                         int64_t lds, uint16_t* __restrict__ dst, int64_t ldd)
+{
+    __shared__ uint16_t tile[32][33];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols)
+            tile[i][threadIdx.x] = src[r * lds + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        if (TRANSPOSE) {
+            const int64_t r = c0 + i, c = r0 + threadIdx.x;  // dst row = src column
+            if (r < cols && c < rows)
+                dst[r * ldd + c] = tile[threadIdx.x][i];
+        } else {
+            const int64_t r = r0 + i, c = c0 + threadIdx.x;
+            if (r < rows && c < cols)
+                dst[r * ldd + c] = tile[i][threadIdx.x];
+        }
+    }
+}
+
 }  // namespace bfp8

@@ -145,8 +145,8 @@ int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, const float* s
  * plainly, with Frobenius norms |.|, U the Newton-Schulz orthogonalisation of
  * the gradient G, learning rate lr and radius R:
  *   X0 = G / (|G| + eps);  W' = W - lr R U / |U|;  W_new = R W' / |W'|.
- * The Newton-Schulz iterations between the two calls are plain BF16 GEMMs
- * (the Python binding runs them through cuBLAS). Sums are deterministic
+ * The Newton-Schulz iterations between the two calls run in the library's BF16
+ * GEMM (muonh_newton_schulz, below). Sums are deterministic
  * (fixed grid, fixed order). Matrices are row-major; cols a multiple of 4.
  *   partials, partials_len: caller-owned scratch of at least
  *     muonh_partials_len() doubles, 8-byte aligned (BFP8_EINVAL if shorter);
@@ -179,6 +179,34 @@ int muonh_apply(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows,
  * to muonh_apply. Arguments and errors otherwise as muonh_apply. */
 int muonh_apply_static(float* w, int64_t ldw, const void* u, int64_t ldu, int64_t rows, int64_t cols,
                        float lr, float radius, void* stream);
+
+/* BF16 GEMM with a scaled sum, the product of the Newton-Schulz iterations below:
+ *   d[m][n] = bf16_rn( alpha * sum_k a[m][k] * B(k, n) + beta * c[m][n] )
+ *   a BF16 [M][K] (lda); b BF16 [N][K] with B(k, n) = b[n][k] (b_mn_major = 0) or
+ *   [K][N] with B(k, n) = b[k][n] (b_mn_major = 1), ldb; c BF16 [M][N] (ldc), read only
+ *   if beta != 0 (may be NULL otherwise); d BF16 [M][N] (ldd). The tensor core sums the
+ *   exact BF16 products in FP32 over the whole contraction; alpha and beta are applied
+ *   in FP32, then one rounding to BF16. M, N, K >= 1, N a multiple of 8 (K and M any).
+ * Alignment: every pointer 16 B, every leading dimension % 8 == 0. d must not overlap
+ * a, b or c. */
+int bf16_gemm_axpby(const void* a, int64_t lda, const void* b, int64_t ldb, int b_mn_major,
+                    const void* c, int64_t ldc, void* d, int64_t ldd, int64_t M, int64_t N, int64_t K,
+                    float alpha, float beta, void* stream);
+
+/* Newton-Schulz orthogonalisation of the MuonH update (the Muon part of MuonH; same
+ * article and section as muonh_normalize), in place on x, BF16 [rows][cols] (ldx):
+ * `steps` quintic iterations X <- a X + (b A + c A A) X with A = X X^T, run on the
+ * orientation with fewer rows (x^T when rows > cols). Each product is one
+ * bf16_gemm_axpby (A and the B = b A + c A A matrix are rounded to BF16, as is X after
+ * each step). rows and cols multiples of 8; x 16-byte aligned, ldx % 8 == 0.
+ *   work, work_bytes: caller scratch of at least muonh_newton_schulz_work_bytes(rows,
+ *     cols) bytes, 16-byte aligned (BFP8_EINVAL if shorter); overwritten by every call,
+ *     so calls that share it must be ordered.
+ * muonh_newton_schulz_work_bytes: writes the scratch size; BFP8_EINVAL for NULL or
+ * sizes < 1. */
+int muonh_newton_schulz_work_bytes(int64_t rows, int64_t cols, int64_t* bytes);
+int muonh_newton_schulz(void* x, int64_t rows, int64_t cols, int64_t ldx, void* work, int64_t work_bytes,
+                        int steps, float a, float b, float c, void* stream);
 
 /* Human-readable name of a bfp8_status value (static string, never NULL). */
 const char* bfp8_status_string(int status);

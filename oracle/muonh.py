@@ -41,6 +41,15 @@ def newton_schulz(X0, steps: int = 5, coeffs=MUON_NS_COEFFS):
     return X.T if t else X
 
 
+def gemm_axpby(A, B, C, alpha: float, beta: float):
+    """alpha * A @ B + beta * C in FP64: one product of the Newton-Schulz iteration (A X^T,
+    b A + c A A, a X + B X are all of this form)."""
+    out = alpha * (np.asarray(A, dtype=np.float64) @ np.asarray(B, dtype=np.float64))
+    if C is not None:
+        out = out + beta * np.asarray(C, dtype=np.float64)
+    return out
+
+
 def apply(W, U, lr: float, radius: float):
     W = np.asarray(W, dtype=np.float64)
     U = np.asarray(U, dtype=np.float64)

@@ -26,7 +26,8 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
                           "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers",
-                          "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static"}
+                          "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static",
+                          "bf16_gemm_axpby", "muonh_newton_schulz_work_bytes", "muonh_newton_schulz"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
     for n in names:
         assert hasattr(cdll, n), n
@@ -131,3 +132,29 @@ def test_muonh_argument_checks(lib):
     assert lib.muonh_normalize(A, 4, 8, 8, A, 8, A, 0, f(0.0), s) != OK
     assert lib.muonh_apply_static(A, 8, A, 8, 4, 8, f(0.1), f(0.0), s) == EINVAL   # radius 0
     assert lib.muonh_apply_static(A, 8, A, 8, 4, 6, f(0.1), f(1.0), s) == ESHAPE   # cols % 4
+
+
+def test_bf16_gemm_and_newton_schulz_argument_checks(lib):
+    import ctypes as ct
+    g = lib.bf16_gemm_axpby
+    f = ct.c_float
+    assert g(A, 64, A, 64, 0, None, 0, A, 64, 0, 64, 64, f(1), f(0), None) == EINVAL       # M < 1
+    assert g(A, 64, A, 64, 2, None, 0, A, 64, 64, 64, 64, f(1), f(0), None) == EINVAL      # bad layout flag
+    assert g(A, 64, A, 64, 0, None, 0, A, 64, 64, 60, 64, f(1), f(0), None) == ESHAPE      # N % 8
+    assert g(A, 64, A, 64, 0, None, 0, A, 64, 64, 64, 64, f(1), f(1), None) == EINVAL      # beta != 0, no C
+    assert g(A, 32, A, 64, 0, None, 0, A, 64, 64, 64, 64, f(1), f(0), None) == EINVAL      # lda < K
+    assert g(A + 8, 64, A, 64, 0, None, 0, A, 64, 64, 64, 64, f(1), f(0), None) == EALIGN  # misaligned a
+    assert g(A, 68, A, 64, 0, None, 0, A, 64, 64, 64, 64, f(1), f(0), None) == EALIGN      # lda % 8
+    n = ct.c_int64(0)
+    assert lib.muonh_newton_schulz_work_bytes(64, 256, ct.byref(n)) == OK
+    # A and B: 64 x 64, two Y buffers: 64 x 256, BF16
+    assert n.value == 2 * (2 * 64 * 64 + 2 * 64 * 256)
+    assert lib.muonh_newton_schulz_work_bytes(256, 64, ct.byref(n)) == OK and n.value == 2 * (2 * 64 * 64 + 2 * 64 * 256)
+    assert lib.muonh_newton_schulz_work_bytes(0, 64, ct.byref(n)) == EINVAL
+    ns = lib.muonh_newton_schulz
+    need = 2 * (2 * 64 * 64 + 2 * 64 * 256)
+    assert ns(A, 64, 256, 256, A, need - 1, 5, f(3.4445), f(-4.775), f(2.0315), None) == EINVAL  # short scratch
+    assert ns(A, 60, 256, 256, A, need, 5, f(3.4445), f(-4.775), f(2.0315), None) == ESHAPE      # rows % 8
+    assert ns(A, 64, 256, 200, A, need, 5, f(3.4445), f(-4.775), f(2.0315), None) == EINVAL      # ldx < cols
+    assert ns(A, 64, 256, 260, A, need, 5, f(3.4445), f(-4.775), f(2.0315), None) == EALIGN      # ldx % 8
+    assert ns(A, 64, 256, 256, A, need, -1, f(3.4445), f(-4.775), f(2.0315), None) == EINVAL     # steps < 0

@@ -79,3 +79,25 @@ def test_zero_step_result_leaves_w_unchanged():
     assert np.linalg.norm(W - (0.25 * 2.0 / np.linalg.norm(U)) * U) == 0.0
     got = muonh.apply(W, U, 0.25, 2.0)
     assert np.array_equal(got, W)
+
+
+def test_gemm_axpby_matches_brute_force():
+    """The oracle's plain product alpha A B + beta C against a triple loop on small inputs."""
+    rng = np.random.default_rng(11)
+    A, B, C = rng.standard_normal((5, 7)), rng.standard_normal((7, 3)), rng.standard_normal((5, 3))
+    want = np.zeros((5, 3))
+    for i in range(5):
+        for j in range(3):
+            want[i, j] = -0.5 * sum(A[i, k] * B[k, j] for k in range(7)) + 2.0 * C[i, j]
+    assert np.allclose(muonh.gemm_axpby(A, B, C, -0.5, 2.0), want, rtol=0, atol=1e-13)
+    assert np.allclose(muonh.gemm_axpby(A, B, None, 1.0, 0.0), A @ B, rtol=0, atol=1e-13)
+
+
+def test_newton_schulz_step_is_three_products():
+    """One iteration written as the three gemm_axpby products the library runs
+    (A = X X^T, B = b A + c A A, X' = a X + B X) equals the oracle's iteration."""
+    X = muonh.normalize(np.random.default_rng(12).standard_normal((24, 40)))
+    A = muonh.gemm_axpby(X, X.T, None, 1.0, 0.0)
+    Bm = muonh.gemm_axpby(A, A, A, c, b)
+    Xn = muonh.gemm_axpby(Bm, X, X, 1.0, a)
+    assert np.allclose(Xn, muonh.newton_schulz(X, 1), rtol=0, atol=1e-13)
