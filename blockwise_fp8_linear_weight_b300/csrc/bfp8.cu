@@ -284,6 +284,44 @@ int run_quant_blocks(const void* x, int64_t R, int64_t C, int64_t ldx, const Qua
     return launch_status();
 }
 
+// Launches the two-layout quantiser without block-wide barriers (quant_dual_kernel):
+// kDualBuffers shared-memory buffers per CTA, kDualCtasPerSm CTAs per SM.
+constexpr int kDualBuffers = 2;
+constexpr int kDualCtasPerSm = 3;
+
+int run_quant_dual(const void* x, int64_t R, int64_t C, int64_t ldx, const QuantArgs& base, cudaStream_t stream)
+{
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    unsigned* status = device_status_ptr(dev);
+    if (!status)
+        return BFP8_ELAUNCH;
+    CUtensorMap tm;
+    if (!make_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(C), static_cast<uint64_t>(R),
+                  static_cast<uint64_t>(ldx) * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return BFP8_ELAUNCH;
+    constexpr int smem = dual_smem_bytes<kDualBuffers>();
+    static std::atomic<bool> attr_set[kMaxDevices];
+    auto kern = quant_dual_kernel<kDualBuffers, kDualCtasPerSm>;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    QuantArgs a = base;
+    a.R = R;
+    a.nblk_c = C / 128;
+    a.nblocks = ((R + 127) / 128) * a.nblk_c;
+    a.status = status;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.stall = g_stall.load(std::memory_order_relaxed);
+    const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * kDualCtasPerSm);
+    kern<<<static_cast<unsigned>(ctas), kDualThreads, smem, stream>>>(tm, a);
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace bfp8
 
@@ -389,7 +427,7 @@ extern "C" int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, i
     qa.ldqt = ldqt;
     qa.st = st;
     qa.ldst = ldst;
-    return run_quant_blocks<MODE_DUAL>(x, R, C, ldx, qa, static_cast<cudaStream_t>(stream));
+    return run_quant_dual(x, R, C, ldx, qa, static_cast<cudaStream_t>(stream));
 }
 
 // =================================================================== GEMMs

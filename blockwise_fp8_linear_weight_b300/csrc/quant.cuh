@@ -307,10 +307,10 @@ __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t
 // encode the current one, so HBM reads overlap the arithmetic.
 //   MODE_ROWS:   1x128 tiles along the columns -> q [R][C], s [C/128][R]
 //   MODE_COLS:   1x128 tiles down the rows     -> qt [C][R128], st [R128/128][C]
-//   MODE_DUAL:   both of the above from one read of x
 //   MODE_WEIGHT: one 128x128 block per scale   -> q [R][C], s [R/128][C/128]
+// (both activation layouts from one read: quant_dual_kernel below)
 // ---------------------------------------------------------------------------
-enum QuantMode { MODE_ROWS = 1, MODE_COLS = 2, MODE_DUAL = 3, MODE_WEIGHT = 4 };
+enum QuantMode { MODE_ROWS = 1, MODE_COLS = 2, MODE_WEIGHT = 4 };
 
 struct QuantArgs {
     int64_t R, nblk_c, nblocks;
@@ -384,7 +384,8 @@ __device__ __forceinline__ void row_tiles8(const uint32_t (*tile)[64], const Sca
     }
 }
 
-// Column pass by warps 4-7 only (while warps 0-3 do the row pass): thread
+// Column pass by warps 4-7 only (while warps 0-3 do the row pass, in
+// quant_dual_kernel): thread
 // t' = t - 128 takes the column pair 32 ((t'/32) % 2) + lane over rows
 // 64 (t'/64) .. +63; the two row halves combine their amax through shared
 // memory behind a barrier of these 128 threads only.
@@ -486,16 +487,6 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         }
         if (MODE == MODE_COLS)
             column_pass(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
-        if (MODE == MODE_DUAL) {
-            // warps 0-3: row tiles (two groups of 8 per half-warp); warps 4-7, at the
-            // same time: transposed tiles; the two only share the block
-            if (tid < 128) {
-                row_tiles8(tile, stab, a, rb, cb, tid >> 4, 8);
-                row_tiles8(tile, stab, a, rb, cb, (tid >> 4) + 64, 8);
-            } else {
-                column_pass_4w(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
-            }
-        }
         if (MODE == MODE_WEIGHT) {
             uint32_t m = 0;
 #pragma unroll
@@ -538,6 +529,101 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         volatile int never = 0;
         for (int k = i; k < issued && k < i + 2; ++k)
             mbar_wait(&full[k & 1], (k >> 1) & 1, &never, a.status, a.wait_ns);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Both layouts from one read of x (MODE_DUAL semantics), without block-wide
+// barriers: a producer warp (warp 8) keeps NB buffers in flight, each with a
+// "full" mbarrier (TMA landed) and an "empty" one (all eight worker warps done
+// with it); warps 0-3 run the row pass and warps 4-7 the transposed pass as in
+// quant_blocks_kernel<MODE_DUAL>, each warp moving on to the next buffer as soon
+// as it is done with the current one. The transposed pass combines its two row
+// halves through a scratch array indexed by the block's parity, so a fast warp
+// can write the next block's partial maxima while a slow one still reads this
+// block's.
+// ---------------------------------------------------------------------------
+constexpr int kDualWorkers = 8;
+constexpr int kDualThreads = 32 * (kDualWorkers + 1);
+
+template <int NB>
+constexpr int dual_smem_bytes()
+{
+    return NB * kQuantTileBytes + 1024;
+}
+
+template <int NB, int MIN_CTAS>
+__global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
+    quant_dual_kernel(const __grid_constant__ CUtensorMap tmX, const QuantArgs a)
+{
+    extern __shared__ uint8_t qsmem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[NB];
+    __shared__ __align__(8) uint64_t empty[NB];
+    __shared__ __align__(16) uint32_t part[2][2][64];
+    __shared__ ScaleTables stab;
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int my_blocks = a.nblocks > first ? static_cast<int>((a.nblocks - 1 - first) / stride + 1) : 0;
+
+    init_scale_tables(stab);
+    if (tid == 0) {
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], kDualWorkers);
+        }
+        abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tmX);
+    }
+    __syncthreads();
+
+    if (warp == kDualWorkers) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            int issued = 0;
+            const int to_issue = a.stall ? 0 : my_blocks;
+            for (int i = 0; i < to_issue; ++i) {
+                const int b = i % NB;
+                // the buffer's previous block (i - NB) has been consumed by every worker
+                if (i >= NB && !mbar_wait(&empty[b], ((i / NB) - 1) & 1, &abort_flag, a.status, a.wait_ns))
+                    break;
+                const int64_t blk = first + static_cast<int64_t>(i) * stride;
+                const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
+                mbar_arrive_expect_tx(&full[b], kQuantTileBytes);
+                tma_load_2d(tiles + b * kQuantTileBytes, &tmX, &full[b], static_cast<int32_t>(cb * 128),
+                            static_cast<int32_t>(rb * 128));
+                ++issued;
+            }
+            // no copy may still be landing in shared memory at exit
+            volatile int never = 0;
+            for (int i = issued - NB < 0 ? 0 : issued - NB; i < issued; ++i)
+                mbar_wait(&full[i % NB], (i / NB) & 1, &never, a.status, a.wait_ns);
+        }
+        return;
+    }
+
+    for (int i = 0; i < my_blocks; ++i) {
+        const int b = i % NB;
+        const int64_t blk = first + static_cast<int64_t>(i) * stride;
+        const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
+        // every worker waits on the same phase, so all of them give up together
+        if (!mbar_wait(&full[b], (i / NB) & 1, &abort_flag, a.status, a.wait_ns))
+            break;
+        const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + b * kQuantTileBytes);
+        if (warp < 4) {
+            row_tiles8(tile, stab, a, rb, cb, tid >> 4, 8);
+            row_tiles8(tile, stab, a, rb, cb, (tid >> 4) + 64, 8);
+        } else {
+            column_pass_4w(tile, part[i & 1], stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[b]);
     }
 }
 

@@ -56,6 +56,7 @@ def test_every_kernel_reports_a_timeout(stalled):
         ("gemm_wgrad_acc", lambda: bfp8.fp8_block_gemm_wgrad_acc(
             layer.qdyt, layer.sdyt, layer.qxt, layer.sxt, lin.M,
             torch.zeros((lin.N, lin.K), dtype=torch.float32, device="cuda"))),
+        ("bf16_gemm", lambda: bfp8.bf16_gemm_axpby(xd, wd, None, 1.0, 0.0)),
     ]
     for name, call in calls:
         call()
