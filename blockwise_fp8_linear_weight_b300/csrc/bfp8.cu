@@ -285,7 +285,8 @@ int run_quant_blocks(const void* x, int64_t R, int64_t C, int64_t ldx, const Qua
 }
 
 // Launches the two-layout quantiser without block-wide barriers (quant_dual_kernel):
-// kDualBuffers shared-memory buffers per CTA, kDualCtasPerSm CTAs per SM.
+// kDualBuffers shared-memory buffers per CTA, kDualCtasPerSm CTAs per SM (measured
+// best of 2 x 3, 3 x 2 and 4 x 1 on the MLP tensors).
 constexpr int kDualBuffers = 2;
 constexpr int kDualCtasPerSm = 3;
 

@@ -533,11 +533,12 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Both layouts from one read of x (MODE_DUAL semantics), without block-wide
+// Both activation layouts from one read of x (the outputs of MODE_ROWS and
+// MODE_COLS together), without block-wide
 // barriers: a producer warp (warp 8) keeps NB buffers in flight, each with a
 // "full" mbarrier (TMA landed) and an "empty" one (all eight worker warps done
-// with it); warps 0-3 run the row pass and warps 4-7 the transposed pass as in
-// quant_blocks_kernel<MODE_DUAL>, each warp moving on to the next buffer as soon
+// with it); warps 0-3 run the row pass and warps 4-7 the transposed pass at the
+// same time, each warp moving on to the next buffer as soon
 // as it is done with the current one. The transposed pass combines its two row
 // halves through a scratch array indexed by the block's parity, so a fast warp
 // can write the next block's partial maxima while a slow one still reads this

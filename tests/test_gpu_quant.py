@@ -115,6 +115,15 @@ def test_full_size_workload_tensors(lin):
     qo, so = oracle.quantize_weight(w)
     _same(q, qo)
     _same(s, so)
+    # both layouts from one read (what a training step calls)
+    for bits in (x, dy):
+        q, s, qt, st = _gpu_dual(bits)
+        qo, so = oracle.quantize_act(bits)
+        qto, sto = oracle.quantize_transpose(bits)
+        _same(q, qo)
+        _same(s, so)
+        _same(qt, qto)
+        _same(st, sto)
 
 
 def test_strided_inputs_and_outputs():
@@ -151,6 +160,26 @@ def test_dual_layouts_edge_shapes(R, C):
     q, s, qt, st = _gpu_dual(x)
     qo, so = oracle.quantize_act(x)
     qto, sto = oracle.quantize_transpose(x)
+    _same(q, qo)
+    _same(s, so)
+    _same(qt, qto)
+    _same(st, sto)
+
+
+def test_dual_layouts_tiny_and_zero_columns():
+    """Column tiles that are all tiny (scales below 2^-60, the pre-scaled quotient path) or all
+    zero, next to row tiles of each kind, through the two-layout call."""
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((300, 384)).astype(np.float32)
+    x[:, 5] *= 1e-39      # BF16 subnormals all down the column
+    x[:, 130] *= 1e-30    # tiny normals
+    x[:, 200] = 0.0
+    x[:, 201] = -0.0
+    x[7, :] *= 1e-39      # a tiny row as well
+    bits = wl.bf16_bits(x)
+    q, s, qt, st = _gpu_dual(bits)
+    qo, so = oracle.quantize_act(bits)
+    qto, sto = oracle.quantize_transpose(bits)
     _same(q, qo)
     _same(s, so)
     _same(qt, qto)
