@@ -305,9 +305,15 @@ int run_quant_dual(const void* x, int64_t R, int64_t C, int64_t ldx, const Quant
         return BFP8_ELAUNCH;
     constexpr int smem = dual_smem_bytes<kDualBuffers>();
     static std::atomic<bool> attr_set[kMaxDevices];
-    auto kern = quant_dual_kernel<kDualBuffers, kDualCtasPerSm>;
+    // 32-byte stores of the transposed codes when every code row starts on a 32-byte boundary
+    const bool st32 = aligned(base.qt, 32) && base.ldqt % 32 == 0;
+    auto kern = st32 ? quant_dual_kernel<kDualBuffers, kDualCtasPerSm, true>
+                     : quant_dual_kernel<kDualBuffers, kDualCtasPerSm, false>;
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(quant_dual_kernel<kDualBuffers, kDualCtasPerSm, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(quant_dual_kernel<kDualBuffers, kDualCtasPerSm, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return BFP8_ELAUNCH;
         attr_set[dev].store(true, std::memory_order_relaxed);
     }

@@ -384,11 +384,23 @@ __device__ __forceinline__ void row_tiles8(const uint32_t (*tile)[64], const Sca
     }
 }
 
+// 32 codes (one column of 32 rows) as one 32-byte store: a whole sector per lane.
+// dst must be 32-byte aligned.
+__device__ __forceinline__ void store_codes32(uint8_t* dst, const uint32_t (&c)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(c[0]), "r"(c[1]),
+                 "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7])
+                 : "memory");
+}
+
 // Column pass by warps 4-7 only (while warps 0-3 do the row pass, in
 // quant_dual_kernel): thread
 // t' = t - 128 takes the column pair 32 ((t'/32) % 2) + lane over rows
 // 64 (t'/64) .. +63; the two row halves combine their amax through shared
 // memory behind a barrier of these 128 threads only.
+// With ST32 every column's 32 codes go out as one 32-byte store (qt and ldqt 32-byte
+// aligned), else as two 16-byte stores.
+template <bool ST32>
 __device__ __forceinline__ void column_pass_4w(const uint32_t (*tile)[64], uint32_t (*part)[64], const ScaleTables& tab,
                                                int64_t cb, int64_t rb, uint8_t* __restrict__ qt, int64_t ldqt,
                                                float* __restrict__ st, int64_t ldst)
@@ -416,10 +428,15 @@ __device__ __forceinline__ void column_pass_4w(const uint32_t (*tile)[64], uint3
             column_encode<true>(tile, 2 * half + q, cw, ps, c0, c1);
         else
             column_encode<false>(tile, 2 * half + q, cw, ps, c0, c1);
-        reinterpret_cast<uint4*>(out0 + 32 * q)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-        reinterpret_cast<uint4*>(out0 + 32 * q)[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
-        reinterpret_cast<uint4*>(out1 + 32 * q)[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
-        reinterpret_cast<uint4*>(out1 + 32 * q)[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+        if constexpr (ST32) {
+            store_codes32(out0 + 32 * q, c0);
+            store_codes32(out1 + 32 * q, c1);
+        } else {
+            reinterpret_cast<uint4*>(out0 + 32 * q)[0] = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+            reinterpret_cast<uint4*>(out0 + 32 * q)[1] = make_uint4(c0[4], c0[5], c0[6], c0[7]);
+            reinterpret_cast<uint4*>(out1 + 32 * q)[0] = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+            reinterpret_cast<uint4*>(out1 + 32 * q)[1] = make_uint4(c1[4], c1[5], c1[6], c1[7]);
+        }
     }
     if (half == 0)
         *reinterpret_cast<float2*>(st + rb * ldst + cb * 128 + col) = make_float2(s0.s, s1.s);
@@ -553,7 +570,7 @@ constexpr int dual_smem_bytes()
     return NB * kQuantTileBytes + 1024;
 }
 
-template <int NB, int MIN_CTAS>
+template <int NB, int MIN_CTAS, bool ST32>
 __global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
     quant_dual_kernel(const __grid_constant__ CUtensorMap tmX, const QuantArgs a)
 {
@@ -620,7 +637,7 @@ __global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
             row_tiles8(tile, stab, a, rb, cb, tid >> 4, 8);
             row_tiles8(tile, stab, a, rb, cb, (tid >> 4) + 64, 8);
         } else {
-            column_pass_4w(tile, part[i & 1], stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+            column_pass_4w<ST32>(tile, part[i & 1], stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
         }
         __syncwarp();
         if (lane == 0)

@@ -166,6 +166,29 @@ def test_dual_layouts_edge_shapes(R, C):
     _same(st, sto)
 
 
+def test_dual_layouts_into_strided_outputs():
+    """The two-layout call into views with padded row strides; a transposed stride that is an odd
+    multiple of 16 bytes takes the 16-byte-store path, a multiple of 32 the 32-byte one. Padding is
+    left untouched."""
+    R, C = 300, 384
+    x = _special_input(R, C, 23)
+    for pad in (16, 32):
+        q = torch.full((R, C + 64), 0xAB, dtype=torch.uint8, device="cuda")
+        s = torch.full((C // 128, R + 4), -1.0, dtype=torch.float32, device="cuda")
+        qt = torch.full((C, 384 + pad), 0xCD, dtype=torch.uint8, device="cuda")
+        st = torch.full((3, C + 4), -1.0, dtype=torch.float32, device="cuda")
+        bfp8.fp8_quantize_act_transpose(to_dev_bf16(x), q[:, :C], s[:, :R], qt[:, :384], st[:, :C])
+        torch.cuda.synchronize()
+        qo, so = oracle.quantize_act(x)
+        qto, sto = oracle.quantize_transpose(x)
+        _same(q[:, :C].cpu().numpy(), qo)
+        _same(s[:, :R].cpu().numpy(), so)
+        _same(qt[:, :384].cpu().numpy(), qto)
+        _same(st[:, :C].cpu().numpy(), sto)
+        assert (q[:, C:].cpu().numpy() == 0xAB).all() and (qt[:, 384:].cpu().numpy() == 0xCD).all()
+        assert (s[:, R:].cpu().numpy() == -1.0).all() and (st[:, C:].cpu().numpy() == -1.0).all()
+
+
 def test_dual_layouts_tiny_and_zero_columns():
     """Column tiles that are all tiny (scales below 2^-60, the pre-scaled quotient path) or all
     zero, next to row tiles of each kind, through the two-layout call."""
