@@ -27,8 +27,9 @@
 //   warp 0      TMA producer of the operand ring;
 //   warp 1      allocates TMEM; one thread issues 4 tcgen05.mma (K = 32 each)
 //               per chunk into one of two TMEM accumulators of BN columns;
-//   warp 2      producer of the scale ring (TMA for the per-row and per-column
-//               scales; plain loads for the scalar B scales);
+//   warp 2      producer of the scale ring (TMA for the per-row A scales; plain
+//               loads for the B scales, shared with warp 3 for per-column ones,
+//               which it stores permuted for the promotion's 16x256b layout);
 //   warps 4..   promotion (8 warps; 12 with 192-wide tiles): warp w owns
 //               TMEM lanes 32 (w%4) .. +31 (output rows) and BN/(PW/4)
 //               columns; per chunk it reads the partial sums with tcgen05.ld
@@ -112,6 +113,9 @@ struct GemmConfig {
     static constexpr int SBS_PER_CHUNK = BN == 128 ? 1 : 2;
     static constexpr uint32_t OP_TX = A_BYTES + B_BYTES;
     static constexpr uint32_t SC_TX = SGROUP * SA_BYTES;  // TMA bytes of one scale stage (A scales)
+    // scale-producer warps: with per-column B scales, warps 2 and 3 each fetch half of
+    // a group's column scales with plain loads, all in flight at once
+    static constexpr int SCALE_WARPS = SB_VEC ? 2 : 1;
     // epilogue staging: per promotion warp CPW/64 boxes of 32 rows x 128 bytes
     // (64 BF16 or 32 FP32 columns; 4 KB, 128-byte swizzle)
     static constexpr int BOX_BYTES = 32 * 128;
@@ -133,9 +137,10 @@ struct GemmConfig {
     // registers per thread at launch (65536 / THREADS, rounded down to a multiple of 8)
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
     // setmaxnreg split between the producer/MMA warpgroup and the two promotion
-    // warpgroups (chosen so that neither side spills on its hot path)
-    static constexpr int REG_LOW = PW_ == 12 ? 56 : 56;
-    static constexpr int REG_HIGH = PW_ == 12 ? 152 : 224;
+    // warpgroups, chosen so that neither side spills (per-column B scales: the
+    // promotion's 16x256b path needs 232, and the producers then fit in 40)
+    static constexpr int REG_LOW = PW_ == 12 ? 56 : (SB_VEC ? 40 : 56);
+    static constexpr int REG_HIGH = PW_ == 12 ? 152 : (SB_VEC ? 232 : 224);
     static_assert(PW_ == 8 || PW_ == 12, "8 or 12 promotion warps");
     static_assert(CPW % 64 == 0, "promotion works on pairs of 32-column quarters");
     static_assert(!REG_SPLIT || 128 * REG_LOW + 32 * PW_ * REG_HIGH <= THREADS * LAUNCH_REGS, "register split");
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&empty[s], 1);  // one MMA completion
         }
         for (int s = 0; s < Cfg::SSTAGES; ++s) {
-            mbar_init(&sfull[s], 1);
+            mbar_init(&sfull[s], Cfg::SCALE_WARPS);  // one arrival per scale-producer warp
             mbar_init(&sempty[s], Cfg::PROMO_WARPS);
         }
         for (int b = 0; b < Cfg::NBUF; ++b) {
@@ -281,8 +286,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int g = issued - Cfg::STAGES < 0 ? 0 : issued - Cfg::STAGES; g < issued; ++g)
                 mbar_wait(&full[g % Cfg::STAGES], (g / Cfg::STAGES) & 1, &never, args.status, args.wait_ns);
         }
-    } else if (warp == 2) {
+    } else if (warp == 2 || (Cfg::SCALE_WARPS == 2 && warp == 3)) {
         // ---------------------------------------------------------------- scale producer
+        const int sp = warp - 2;  // this warp's share of the per-column scales
         // Groups of SGROUP chunks of one tile (the last group of a tile may be
         // shorter: TMA fills the rows past the last chunk with zeros, and the
         // promotion warps never read them).
@@ -306,12 +312,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 if constexpr (Cfg::SB_VEC) {
-                    // the group's per-column scales, a column pair per lane and step,
-                    // written in the promotion's permuted layout (zero past the edges)
+                    // this warp's half of the group's per-column scales, a column pair
+                    // per lane and step, written in the promotion's permuted layout
+                    // (zero past the edges)
                     float* dst = sSB + qs * Cfg::SGROUP * Cfg::SBV_CHUNK;
                     constexpr int PAIRS = Cfg::BN / 2;
+                    constexpr int HALF = Cfg::SGROUP * PAIRS / 2;
+                    static_assert(HALF % 32 == 0, "whole steps of 32 column pairs");
 #pragma unroll 4
-                    for (int u = lane; u < Cfg::SGROUP * PAIRS; u += 32) {
+                    for (int k = 0; k < HALF / 32; ++k) {
+                        const int u = sp * HALF + lane + 32 * k;
                         const int cc = u / PAIRS, n = 2 * (u % PAIRS);
                         const int c = c0 + cc;
                         float2 v = make_float2(0.0f, 0.0f);
@@ -337,14 +347,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     __syncwarp();  // the stores above happen before lane 0's arrive (release)
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&sfull[qs], Cfg::SC_TX);
-                    tma_load_2d(sSA + qs * Cfg::SGROUP * Cfg::BM, &tmSA, &sfull[qs], m0, c0);
+                    if (sp == 0) {
+                        mbar_arrive_expect_tx(&sfull[qs], Cfg::SC_TX);
+                        tma_load_2d(sSA + qs * Cfg::SGROUP * Cfg::BM, &tmSA, &sfull[qs], m0, c0);
+                    } else {
+                        mbar_arrive(&sfull[qs]);
+                    }
                 }
                 ++issued;
             }
         }
-        // no copy may still be landing in shared memory at exit
-        if (lane == 0) {
+        // no copy may still be landing in shared memory at exit (warp 2 issued them)
+        if (lane == 0 && sp == 0) {
             volatile int never = 0;
             for (int q = issued - Cfg::SSTAGES < 0 ? 0 : issued - Cfg::SSTAGES; q < issued; ++q)
                 mbar_wait(&sfull[q % Cfg::SSTAGES], (q / Cfg::SSTAGES) & 1, &never, args.status, args.wait_ns);
