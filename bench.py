@@ -315,10 +315,13 @@ class Case:
         self.bfp8, self.torch, self.work = bfp8, torch, work
         self.fwd_only = work.passes == ("fwd",)
         self.layers, self.inputs, by_shape = [], [], {}
+        # one GEMM workspace for all layers: they run one after another on one stream
+        self.workspace = bfp8.gemm_workspace(dev)
+        self._kernels_per_step = None
         for lin in work.linears:
             key = (lin.M, lin.K, lin.N)
             if key not in by_shape:
-                by_shape[key] = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev)
+                by_shape[key] = bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev, workspace=self.workspace)
             self.layers.append(by_shape[key])
             if source == "numpy":
                 self.inputs.append(tuple(torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -328,7 +331,12 @@ class Case:
 
     @property
     def kernels_per_step(self):
-        return sum(3 if self.fwd_only else L.KERNELS_PER_STEP for L in self.layers)
+        """The library's kernel launches in one step, counted by the library itself."""
+        if self._kernels_per_step is None:
+            n0 = self.bfp8.kernel_launches()
+            self.step()
+            self._kernels_per_step = self.bfp8.kernel_launches() - n0
+        return self._kernels_per_step
 
     def step(self, mark=None):
         """One training step of every linear; mark(tag, work) after each kernel if given."""
@@ -344,15 +352,15 @@ class Case:
                 mark("quant_act_transpose", dual_bytes(M, K))
             b.fp8_quantize_weight(w, L.qw, L.sw)
             mark("quant_weight", quant_bytes(N, K))
-            b.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+            b.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y, workspace=L.workspace)
             mark("gemm_fwd", 2 * M * N * K)
             if self.fwd_only:
                 continue
             b.fp8_quantize_act_transpose(dy, L.qdy, L.sdy, L.qdyt, L.sdyt)
             mark("quant_act_transpose", dual_bytes(M, N))
-            b.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx)
+            b.fp8_block_gemm_dgrad(L.qdy, L.sdy, L.qw, L.sw, L.dx, workspace=L.workspace)
             mark("gemm_dgrad", 2 * M * N * K)
-            b.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw)
+            b.fp8_block_gemm_wgrad(L.qdyt, L.sdyt, L.qxt, L.sxt, M, L.dw, workspace=L.workspace)
             mark("gemm_wgrad", 2 * M * N * K)
 
 
@@ -571,7 +579,7 @@ def end_to_end(bfp8, torch, case: Case, host, dev, ws: int, steps: int):
     work, layers = case.work, case.layers
     fwd_only = case.fwd_only
     sets = [[(tuple(torch.empty_like(t, device=dev) for t in h),
-              bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev) if k else L)
+              bfp8.BlockwiseFP8Linear(lin.M, lin.K, lin.N, dev, workspace=case.workspace) if k else L)
              for h, lin, L in zip(host, work.linears, layers)] for k in range(2)]
     outs_host = [tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (L.y, L.dx, L.dw))
                  for L in layers]
@@ -602,7 +610,7 @@ def end_to_end(bfp8, torch, case: Case, host, dev, ws: int, steps: int):
                 if fwd_only:
                     bfp8.fp8_quantize_act(d[0], L.qx, L.sx)
                     bfp8.fp8_quantize_weight(d[1], L.qw, L.sw)
-                    bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y)
+                    bfp8.fp8_block_gemm_fwd(L.qx, L.sx, L.qw, L.sw, L.y, workspace=L.workspace)
                 else:
                     L.forward(d[0], d[1])
                     L.backward(d[2])
@@ -745,13 +753,17 @@ def side_measurements(bfp8, torch, case: Case, stream, fp8_peak, fp8_tflops, ste
             L.forward(x, w)
             L.backward(dy)
 
+    n0 = bfp8.kernel_launches()
+    reuse_step()
+    k_reuse = bfp8.kernel_launches() - n0
+    torch.cuda.synchronize()
     g = capture(torch, reuse_step)
     ms_reuse = replay_ms(torch, g, steps, stream) / steps
     for L in layers:
         L.reuse_weight_quant = False
     out["weight_quant_reuse"] = {"tflops": round(work.flops / (ms_reuse / 1e3) / 1e12, 1),
                                  "ms_per_step": round(ms_reuse, 4),
-                                 "kernels_per_step": 5 * len(layers), "what": "graph replays"}
+                                 "kernels_per_step": k_reuse, "what": "graph replays"}
     # MuonH: every linear's weight gets one optimizer step per iteration
     mw = [(torch.randn((l.N, l.K), device=dev) * 0.02).float() for l in work.linears]
     mg = [torch.randn((l.N, l.K), device=dev) for l in work.linears]

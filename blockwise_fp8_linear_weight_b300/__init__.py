@@ -14,6 +14,8 @@ Entry points (same names as the C ABI):
   fp8_block_gemm_fwd(qx, sx, qw, sw)        -> y  [M, N] bf16
   fp8_block_gemm_dgrad(qdy, sdy, qw, sw)    -> dx [M, K] bf16
   fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M) -> dw [N, K] bf16
+    (each takes an optional workspace=gemm_workspace(): the split of the grid's
+    last partial round of tiles along the contraction axis)
   fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad): main_grad [N, K] f32 += dW
 MuonH (one optimizer step for one weight matrix):
   muonh_update(w, g, lr, radius)  # w FP32 in place; see muonh_update's docstring
@@ -65,14 +67,16 @@ def load_library(path: str = LIB_PATH):
         "fp8_quantize_weight": [p, i64, i64, i64, p, i64, p, p],
         "fp8_quantize_transpose": [p, i64, i64, i64, p, i64, p, i64, p],
         "fp8_quantize_act_transpose": [p, i64, i64, i64, p, i64, p, i64, p, i64, p, i64, p],
-        "fp8_block_gemm_fwd": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
-        "fp8_block_gemm_dgrad": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p],
-        "fp8_block_gemm_wgrad": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
+        "fp8_block_gemm_workspace_bytes": [ctypes.POINTER(i64)],
+        "fp8_block_gemm_fwd": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p, i64, p],
+        "fp8_block_gemm_dgrad": [p, i64, p, i64, p, i64, p, p, i64, i64, i64, i64, p, i64, p],
+        "fp8_block_gemm_wgrad": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p, i64, p],
         "fp8_block_gemm_wgrad_acc": [p, i64, p, i64, p, i64, p, i64, p, i64, i64, i64, i64, p],
         "bfp8_last_device_status": [p],
         "bfp8_set_gemm_tile_n": [c_int],
         "bfp8_set_wait_limit_ns": [i64],
         "bfp8_test_stall_producers": [c_int],
+        "bfp8_kernel_launches": [ctypes.POINTER(i64)],
         "muonh_partials_len": [ctypes.POINTER(c_int)],
         "muonh_normalize": [p, i64, i64, i64, p, i64, p, i64, ctypes.c_float, p],
         "muonh_apply": [p, i64, p, i64, i64, i64, p, i64, ctypes.c_float, ctypes.c_float, p],
@@ -192,39 +196,63 @@ def fp8_quantize_act_transpose(x, q=None, s=None, qt=None, st=None):
 
 
 # ----------------------------------------------------------------------- GEMMs
-def fp8_block_gemm_fwd(qx, sx, qw, sw, y=None):
+def gemm_workspace_bytes() -> int:
+    """Workspace size that lets the GEMMs split their last partial round of tiles (current device)."""
+    n = ctypes.c_int64(0)
+    _check("fp8_block_gemm_workspace_bytes", load_library().fp8_block_gemm_workspace_bytes(ctypes.byref(n)))
+    return n.value
+
+
+def gemm_workspace(device="cuda"):
+    """A GEMM workspace (uint8 CUDA tensor) for the device; calls sharing one must be stream-ordered."""
+    with torch.cuda.device(torch.device(device)):
+        return torch.empty(gemm_workspace_bytes(), dtype=torch.uint8, device=device)
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def fp8_block_gemm_fwd(qx, sx, qw, sw, y=None, workspace=None):
     """y [M, N] bf16 = blockwise-FP8 x W^T from (qx [M,K], sx [K/128, M], qw [N,K], sw [N/128, K/128])."""
     lib = load_library()
     M, K = qx.shape
     N = qw.shape[0]
     y = torch.empty((M, N), dtype=torch.bfloat16, device=qx.device) if y is None else y
+    ws, ws_bytes = _ws(workspace)
     _check("fp8_block_gemm_fwd", lib.fp8_block_gemm_fwd(
         _ptr(qx), qx.stride(0), _ptr(sx), sx.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
-        _ptr(y), y.stride(0), M, N, K, _stream()))
+        _ptr(y), y.stride(0), M, N, K, ws, ws_bytes, _stream()))
     return y
 
 
-def fp8_block_gemm_dgrad(qdy, sdy, qw, sw, dx=None):
+def fp8_block_gemm_dgrad(qdy, sdy, qw, sw, dx=None, workspace=None):
     """dx [M, K] bf16 = blockwise-FP8 dy W from (qdy [M,N], sdy [N/128, M], qw [N,K], sw [N/128, K/128])."""
     lib = load_library()
     M, N = qdy.shape
     K = qw.shape[1]
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=qdy.device) if dx is None else dx
+    ws, ws_bytes = _ws(workspace)
     _check("fp8_block_gemm_dgrad", lib.fp8_block_gemm_dgrad(
         _ptr(qdy), qdy.stride(0), _ptr(sdy), sdy.stride(0), _ptr(qw), qw.stride(0), _ptr(sw),
-        _ptr(dx), dx.stride(0), M, N, K, _stream()))
+        _ptr(dx), dx.stride(0), M, N, K, ws, ws_bytes, _stream()))
     return dx
 
 
-def fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M, dw=None):
+def fp8_block_gemm_wgrad(qdyt, sdyt, qxt, sxt, M, dw=None, workspace=None):
     """dw [N, K] bf16 = blockwise-FP8 dy^T x from transposed tiles (qdyt [N,M128], qxt [K,M128])."""
     lib = load_library()
     N = qdyt.shape[0]
     K = qxt.shape[0]
     dw = torch.empty((N, K), dtype=torch.bfloat16, device=qdyt.device) if dw is None else dw
+    ws, ws_bytes = _ws(workspace)
     _check("fp8_block_gemm_wgrad", lib.fp8_block_gemm_wgrad(
         _ptr(qdyt), qdyt.stride(0), _ptr(sdyt), sdyt.stride(0), _ptr(qxt), qxt.stride(0),
-        _ptr(sxt), sxt.stride(0), _ptr(dw), dw.stride(0), M, N, K, _stream()))
+        _ptr(sxt), sxt.stride(0), _ptr(dw), dw.stride(0), M, N, K, ws, ws_bytes, _stream()))
     return dw
 
 
@@ -238,6 +266,13 @@ def fp8_block_gemm_wgrad_acc(qdyt, sdyt, qxt, sxt, M, main_grad):
         _ptr(qdyt), qdyt.stride(0), _ptr(sdyt), sdyt.stride(0), _ptr(qxt), qxt.stride(0),
         _ptr(sxt), sxt.stride(0), _ptr(main_grad), main_grad.stride(0), M, N, K, _stream()))
     return main_grad
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far (host-side count)."""
+    n = ctypes.c_int64(0)
+    _check("bfp8_kernel_launches", load_library().bfp8_kernel_launches(ctypes.byref(n)))
+    return n.value
 
 
 def last_device_status() -> int:
@@ -275,8 +310,9 @@ class BlockwiseFP8Linear:
     forward GEMM, 1x128 along M, transposed, for the weight-gradient GEMM) and
     W (128x128), then runs the forward GEMM; ``backward(dy)`` quantises dy in
     both layouts and runs the input- and weight-gradient GEMMs. All outputs
-    live in buffers allocated once, so a training step launches exactly six
-    kernels and allocates nothing.
+    live in buffers allocated once, so a training step launches six kernels
+    (plus one tail-reduce kernel per GEMM whose last round of tiles is split)
+    and allocates nothing.
 
     Options:
       reuse_weight_quant: keep W's codes and scales while W is unchanged (same
@@ -288,12 +324,14 @@ class BlockwiseFP8Linear:
         (``self.main_grad``, zeroed by ``zero_main_grad()``) instead of writing
         a BF16 dW, as a trainer keeping its state in FP32 does across
         micro-batches.
+      workspace: the GEMM workspace (``gemm_workspace()``, 38 MB on a B300)
+        that lets each GEMM split the grid's last partial round of tiles along
+        the contraction axis; layers that run one after another on one stream
+        may share one. None: allocate one for this layer. False: no split.
     """
 
-    KERNELS_PER_STEP = 6
-
     def __init__(self, M: int, K: int, N: int, device="cuda", reuse_weight_quant: bool = False,
-                 main_grad: bool = False):
+                 main_grad: bool = False, workspace=None):
         self.M, self.K, self.N = M, K, N
         self.reuse_weight_quant = reuse_weight_quant
         self.weight_quant_calls = 0
@@ -315,6 +353,9 @@ class BlockwiseFP8Linear:
         self.dx = torch.empty((M, K), dtype=bf, device=dev)
         self.dw = None if main_grad else torch.empty((N, K), dtype=bf, device=dev)
         self.main_grad = torch.zeros((N, K), dtype=f32, device=dev) if main_grad else None
+        if workspace is None:
+            workspace = gemm_workspace(dev)
+        self.workspace = workspace if workspace is not False else None
 
     def quantize_weight(self, w):
         """Quantise W unless reuse is on and W is the tensor (and version) quantised last."""
@@ -335,17 +376,18 @@ class BlockwiseFP8Linear:
     def forward(self, x, w):
         fp8_quantize_act_transpose(x, self.qx, self.sx, self.qxt, self.sxt)
         self.quantize_weight(w)
-        fp8_block_gemm_fwd(self.qx, self.sx, self.qw, self.sw, self.y)
+        fp8_block_gemm_fwd(self.qx, self.sx, self.qw, self.sw, self.y, workspace=self.workspace)
         return self.y
 
     def backward(self, dy):
         """Returns (dx, dW): dW is the BF16 buffer, or the FP32 main gradient it was added into."""
         fp8_quantize_act_transpose(dy, self.qdy, self.sdy, self.qdyt, self.sdyt)
-        fp8_block_gemm_dgrad(self.qdy, self.sdy, self.qw, self.sw, self.dx)
+        fp8_block_gemm_dgrad(self.qdy, self.sdy, self.qw, self.sw, self.dx, workspace=self.workspace)
         if self.main_grad is not None:
             fp8_block_gemm_wgrad_acc(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.main_grad)
             return self.dx, self.main_grad
-        fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw)
+        fp8_block_gemm_wgrad(self.qdyt, self.sdyt, self.qxt, self.sxt, self.M, self.dw,
+                             workspace=self.workspace)
         return self.dx, self.dw
 
 

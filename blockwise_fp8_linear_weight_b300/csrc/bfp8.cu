@@ -121,6 +121,14 @@ int launch_status()
     return cudaGetLastError() == cudaSuccess ? BFP8_OK : BFP8_ELAUNCH;
 }
 
+// Kernels launched by the library in this process (bfp8_kernel_launches).
+std::atomic<int64_t> g_launches{0};
+
+void note_launch()
+{
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+}
+
 // ----------------------------------------------------------------- GEMM launch
 struct GemmProblem {
     // A: codes [gm][ld_a] with the contraction axis (gk) contiguous
@@ -141,7 +149,25 @@ struct GemmProblem {
     void* d;
     int64_t ldd;
     int64_t gm, gn, gk;
+    // caller workspace for the split tail (NULL: no split)
+    float* ws;
+    int64_t ws_bytes;
 };
+
+// A tail is split along the contraction axis only when it would leave at least a
+// quarter of the grid idle and the split shortens the longest CTA's tail by at
+// least this many chunks. Measured on the MLP GEMMs of a B300 (20 launches in a
+// CUDA graph): the piece-mode launch runs its chunks at 1.3-2x the whole-tile
+// time per chunk (its own start-up and the partial-tile stores) and the reduce
+// adds about 6 us, so a split that saves 25 chunks lost up to 4 %, one that
+// saves 51 chunks of the weight gradient gained 9 %.
+constexpr int64_t kTailMinSaved = 40;
+
+// Workspace of the split tail: two FP32 partial tiles of 128 x 256 per CTA.
+int64_t tail_ws_bytes(int ctas)
+{
+    return 2LL * ctas * 128 * 256 * 4;
+}
 
 template <class Cfg>
 int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int dev)
@@ -170,19 +196,22 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
         return BFP8_ELAUNCH;
 
     static std::atomic<bool> attr_set[kMaxDevices];
-    auto kern = bfp8_gemm_kernel<Cfg>;
+    auto kern = bfp8_gemm_kernel<Cfg, false>;
+    auto kern_pieces = bfp8_gemm_kernel<Cfg, true>;
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-            cudaSuccess)
-            return BFP8_ELAUNCH;
-        // The register split (setmaxnreg) only balances if the kernel was built
-        // with the full per-thread budget; with fewer registers the promotion
-        // warpgroups' setmaxnreg.inc could never be satisfied. Refuse to launch.
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
-            return BFP8_ELAUNCH;
-        if (Cfg::REG_SPLIT && fa.numRegs < Cfg::LAUNCH_REGS)
-            return BFP8_ELAUNCH;
+        for (auto k : {kern, kern_pieces}) {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+                cudaSuccess)
+                return BFP8_ELAUNCH;
+            // The register split (setmaxnreg) only balances if the kernel was built
+            // with the full per-thread budget; with fewer registers the promotion
+            // warpgroups' setmaxnreg.inc could never be satisfied. Refuse to launch.
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, k) != cudaSuccess)
+                return BFP8_ELAUNCH;
+            if (Cfg::REG_SPLIT && fa.numRegs < Cfg::LAUNCH_REGS)
+                return BFP8_ELAUNCH;
+        }
         attr_set[dev].store(true, std::memory_order_relaxed);
     }
     GemmArgs args;
@@ -203,9 +232,82 @@ int run_gemm(const GemmProblem& p, unsigned* status, cudaStream_t stream, int de
     args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     args.stall = g_stall.load(std::memory_order_relaxed);
     // persistent grid: one CTA per SM, or one per tile if there are fewer tiles
+    const int sms = sm_count(dev);
     const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
-    const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
-    kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmD, args);
+    int ctas = static_cast<int>(std::min<int64_t>(tiles, sms));
+    int64_t tail_tile0 = tiles, units = 0;
+    if (Cfg::EPI != EPI_F32_ADD && p.ws && nc > kTailMinSaved) {
+        // whole rounds of the grid, then a tail split along the contraction axis
+        const int64_t rounds = tiles / sms, rest = tiles - rounds * sms;
+        if (rest > 0 && rest * 4 <= static_cast<int64_t>(sms) * 3) {
+            const int64_t g = rounds > 0 ? sms : std::min<int64_t>(rest * nc, sms);
+            const int64_t longest = (rest * nc + g - 1) / g;  // chunks of the longest tail range
+            // (the reduce kernel lists at most 256 pieces per tile: one per CTA)
+            if (nc - longest >= kTailMinSaved && g <= 256 && p.ws_bytes >= tail_ws_bytes(static_cast<int>(g))) {
+                tail_tile0 = rounds * sms;
+                units = rest * nc;
+                ctas = static_cast<int>(g);
+            }
+        }
+    }
+    args.tail_tile0 = static_cast<int>(tail_tile0);
+    args.tail_units = units;
+    // a launch that may start before the one before it on the stream has finished
+    // (programmatic dependent launch); the kernels wait inside where they need to
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    if (units == 0) {
+        CUtensorMap unused = tmD;
+        kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmD, unused, args);
+        note_launch();
+        return launch_status();
+    }
+    // the whole rounds (if any), then the tail's pieces on the SMs that they free,
+    // then the sum of the partial tiles
+    if (tail_tile0 > 0) {
+        CUtensorMap unused = tmD;
+        kern<<<sms, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmSA, tmD, unused, args);
+        note_launch();
+    }
+    // partial tiles: FP32 [2 ctas x 128 rows][BN], 32 x 32 boxes
+    CUtensorMap tmW;
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.ws, Cfg::BN, 2 * static_cast<uint64_t>(ctas) * Cfg::BM,
+                  Cfg::BN * 4, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+        return BFP8_ELAUNCH;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(ctas));
+    lc.blockDim = dim3(Cfg::THREADS);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = tail_tile0 > 0 ? 1 : 0;
+    if (cudaLaunchKernelEx(&lc, kern_pieces, tmA, tmB, tmSA, tmD, tmW, args) != cudaSuccess)
+        return BFP8_ELAUNCH;
+    note_launch();
+    TailReduceArgs ra;
+    ra.ws = p.ws;
+    ra.d = static_cast<uint16_t*>(p.d);
+    ra.ldd = p.ldd;
+    ra.gm = args.gm;
+    ra.gn = args.gn;
+    ra.num_chunks = args.num_chunks;
+    ra.tail_tile0 = args.tail_tile0;
+    ra.grid = ctas;
+    ra.tail_units = units;
+    ra.tiles_m = args.tiles_m;
+    ra.tiles_n = args.tiles_n;
+    ra.n_fastest = args.n_fastest;
+    cudaLaunchConfig_t lr = {};
+    lr.gridDim = dim3(static_cast<unsigned>(tiles - tail_tile0), Cfg::BM / 8);
+    lr.blockDim = dim3(256);
+    lr.dynamicSmemBytes = 0;
+    lr.stream = stream;
+    lr.attrs = pdl;
+    lr.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lr, gemm_tail_reduce_kernel<Cfg::BN>, ra) != cudaSuccess)
+        return BFP8_ELAUNCH;
+    note_launch();
     return launch_status();
 }
 
@@ -281,6 +383,7 @@ int run_quant_blocks(const void* x, int64_t R, int64_t C, int64_t ldx, const Qua
     a.stall = g_stall.load(std::memory_order_relaxed);
     const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * 3);
     kern<<<static_cast<unsigned>(ctas), 256, kQuantSmemBytes, stream>>>(tm, a);
+    note_launch();
     return launch_status();
 }
 
@@ -326,6 +429,7 @@ int run_quant_dual(const void* x, int64_t R, int64_t C, int64_t ldx, const Quant
     a.stall = g_stall.load(std::memory_order_relaxed);
     const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * kDualCtasPerSm);
     kern<<<static_cast<unsigned>(ctas), kDualThreads, smem, stream>>>(tm, a);
+    note_launch();
     return launch_status();
 }
 
@@ -440,7 +544,8 @@ extern "C" int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, i
 // =================================================================== GEMMs
 extern "C" int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* sx, int64_t ldsx,
                                   const uint8_t* qw, int64_t ldqw, const float* sw, void* y, int64_t ldy,
-                                  int64_t M, int64_t N, int64_t K, void* stream)
+                                  int64_t M, int64_t N, int64_t K, void* workspace, int64_t workspace_bytes,
+                                  void* stream)
 {
     if (M < 0 || N < 0 || K < 0)
         return BFP8_EINVAL;
@@ -453,7 +558,11 @@ extern "C" int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* 
     if (!aligned(qx, 16) || !aligned(qw, 16) || !aligned(sx, 16) || !aligned(y, 16) || !aligned(sw, 4) ||
         ldqx % 16 || ldqw % 16 || ldsx % 4 || ldy % 8)
         return BFP8_EALIGN;
+    if (workspace_bytes < 0 || (workspace && !aligned(workspace, 16)))
+        return workspace_bytes < 0 ? BFP8_EINVAL : BFP8_EALIGN;
     GemmProblem p{};
+    p.ws = static_cast<float*>(workspace);
+    p.ws_bytes = workspace ? workspace_bytes : 0;
     p.a = qx;
     p.lda = ldqx;
     p.b = qw;
@@ -475,7 +584,8 @@ extern "C" int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* 
 
 extern "C" int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const float* sdy, int64_t ldsdy,
                                     const uint8_t* qw, int64_t ldqw, const float* sw, void* dx, int64_t lddx,
-                                    int64_t M, int64_t N, int64_t K, void* stream)
+                                    int64_t M, int64_t N, int64_t K, void* workspace, int64_t workspace_bytes,
+                                    void* stream)
 {
     if (M < 0 || N < 0 || K < 0)
         return BFP8_EINVAL;
@@ -488,7 +598,11 @@ extern "C" int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const flo
     if (!aligned(qdy, 16) || !aligned(qw, 16) || !aligned(sdy, 16) || !aligned(dx, 16) || !aligned(sw, 4) ||
         ldqdy % 16 || ldqw % 16 || ldsdy % 4 || lddx % 8)
         return BFP8_EALIGN;
+    if (workspace_bytes < 0 || (workspace && !aligned(workspace, 16)))
+        return workspace_bytes < 0 ? BFP8_EINVAL : BFP8_EALIGN;
     GemmProblem p{};
+    p.ws = static_cast<float*>(workspace);
+    p.ws_bytes = workspace ? workspace_bytes : 0;
     p.a = qdy;
     p.lda = ldqdy;
     p.b = qw;  // [N][K]: contraction (N) strided, output columns (K) contiguous
@@ -510,7 +624,8 @@ extern "C" int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const flo
 
 extern "C" int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
                                     const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt, void* dw,
-                                    int64_t lddw, int64_t M, int64_t N, int64_t K, void* stream)
+                                    int64_t lddw, int64_t M, int64_t N, int64_t K, void* workspace,
+                                    int64_t workspace_bytes, void* stream)
 {
     if (M < 0 || N < 0 || K < 0)
         return BFP8_EINVAL;
@@ -523,7 +638,11 @@ extern "C" int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const f
     if (!aligned(qdyt, 16) || !aligned(qxt, 16) || !aligned(sdyt, 16) || !aligned(sxt, 16) || !aligned(dw, 16) ||
         ldqdyt % 16 || ldqxt % 16 || ldsdyt % 4 || ldsxt % 4 || lddw % 8)
         return BFP8_EALIGN;
+    if (workspace_bytes < 0 || (workspace && !aligned(workspace, 16)))
+        return workspace_bytes < 0 ? BFP8_EINVAL : BFP8_EALIGN;
     GemmProblem p{};
+    p.ws = static_cast<float*>(workspace);
+    p.ws_bytes = workspace ? workspace_bytes : 0;
     p.a = qdyt;
     p.lda = ldqdyt;
     p.b = qxt;
@@ -577,6 +696,26 @@ extern "C" int fp8_block_gemm_wgrad_acc(const uint8_t* qdyt, int64_t ldqdyt, con
     return dispatch_gemm<false, true, EPI_F32_ADD>(p, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int bfp8_kernel_launches(int64_t* count)
+{
+    if (!count)
+        return BFP8_EINVAL;
+    *count = g_launches.load(std::memory_order_relaxed);
+    return BFP8_OK;
+}
+
+extern "C" int fp8_block_gemm_workspace_bytes(int64_t* bytes)
+{
+    if (!bytes)
+        return BFP8_EINVAL;
+    int dev = 0;
+    const int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    *bytes = tail_ws_bytes(sm_count(dev));
+    return BFP8_OK;
+}
+
 // =================================================================== MuonH
 namespace bfp8 {
 namespace {
@@ -625,8 +764,10 @@ extern "C" int muonh_normalize(const float* g, int64_t rows, int64_t cols, int64
         return BFP8_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     muonh_sumsq_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials);
+    note_launch();
     muonh_scale_bf16_kernel<<<grid, kMuonThreads, 0, st>>>(g, rows, cols, ldg, partials, grid, eps,
                                                           static_cast<uint16_t*>(x), ldx);
+    note_launch();
     return launch_status();
 }
 
@@ -660,8 +801,11 @@ static int muonh_apply_impl(float* w, int64_t ldw, const void* u, int64_t ldu, i
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* ub = static_cast<const uint16_t*>(u);
     muonh_sumsq_u_kernel<<<grid, kMuonThreads, 0, st>>>(ub, ldu, rows, cols, partials);
+    note_launch();
     muonh_wprime_sumsq_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
+    note_launch();
     muonh_apply_kernel<<<grid, kMuonThreads, 0, st>>>(w, ldw, ub, ldu, rows, cols, partials, grid, lr, radius);
+    note_launch();
     return launch_status();
 }
 
@@ -788,6 +932,7 @@ int run_bf16_gemm(const void* a, int64_t lda, const void* b, int64_t ldb, const 
     const int64_t tiles = static_cast<int64_t>(args.tiles_m) * args.tiles_n;
     const int ctas = static_cast<int>(std::min<int64_t>(tiles, sm_count(dev)));
     kern<<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmD, args);
+    note_launch();
     return launch_status();
 }
 
@@ -878,6 +1023,7 @@ extern "C" int muonh_newton_schulz(void* x, int64_t rows, int64_t cols, int64_t 
         bf16_copy_kernel<true><<<grid_in, blk, 0, st>>>(xs, rows, cols, ldx, Y[0], ldc);
     else
         bf16_copy_kernel<false><<<grid_in, blk, 0, st>>>(xs, rows, cols, ldx, Y[0], ldc);
+    note_launch();
     if ((rc = launch_status()) != BFP8_OK)
         return rc;
     int cur = 0;
@@ -900,5 +1046,6 @@ extern "C" int muonh_newton_schulz(void* x, int64_t rows, int64_t cols, int64_t 
         bf16_copy_kernel<true><<<grid_out, blk, 0, st>>>(Y[cur], r, cc, ldc, xs, ldx);
     else
         bf16_copy_kernel<false><<<grid_out, blk, 0, st>>>(Y[cur], r, cc, ldc, xs, ldx);
+    note_launch();
     return launch_status();
 }

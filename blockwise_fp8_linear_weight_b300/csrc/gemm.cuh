@@ -14,7 +14,18 @@
 //
 // Persistent kernel, one CTA per SM, output tiles of 128 x BN visited in a
 // static round-robin order (the smaller operand is re-read from L2, the larger
-// one streamed once). Two shared-memory rings:
+// one streamed once). When the tiles do not fill the last round of the grid,
+// that last partial round (the tail) can be split along the contraction axis:
+// the whole rounds run in one launch, and a second launch of the same kernel
+// in piece mode (SPLIT) cuts the tail tiles' chunks into one contiguous range
+// per CTA. Its CTAs start on the SMs that the first launch frees (a
+// programmatic dependent launch: the pieces need nothing from the whole
+// tiles). A piece that covers a whole tile is stored as usual; every other
+// piece is stored as an FP32 partial tile in a caller workspace, two slots per
+// CTA (its first and its last tail tile), and gemm_tail_reduce_kernel adds
+// the partial tiles of each split tile in CTA order and stores it in BF16. So
+// the tail costs about (tail tiles / CTAs) of a round instead of a whole one,
+// and the result is deterministic. Two shared-memory rings:
 //   operand ring (STAGES deep): the A tile 128x128 and the B tile (BNx128
 //     K-major, or 128-column boxes of an MN-major operand) of one chunk; a
 //     stage is handed back to the producer by the MMA completion alone;
@@ -157,7 +168,22 @@ struct GemmArgs {
     unsigned* status;
     unsigned long long wait_ns;  // limit of one mbarrier wait
     int stall;                   // test switch: the operand producer issues no copies
+    // Tiles 0 .. tail_tile0 - 1 are whole tiles, handed out round-robin by the
+    // whole-tile launch. The piece-mode launch cuts the tail_units =
+    // (tiles - tail_tile0) * num_chunks chunks of the other tiles into gridDim.x
+    // equal contiguous ranges; pieces that are not a whole tile go to ws as FP32
+    // partial tiles, [2 * gridDim.x][BM][BN] row-major (through the tensor map
+    // tmW): slot 2i for CTA i's first tail tile, 2i + 1 for its last one.
+    int tail_tile0;
+    long long tail_units;
 };
+
+// The tail range of chunk units of CTA `cta` out of `ncta`.
+__host__ __device__ __forceinline__ void tail_range(long long units, int cta, int ncta, long long& u0, long long& u1)
+{
+    u0 = units * cta / ncta;
+    u1 = units * (cta + 1) / ncta;
+}
 
 // Origin of the t-th tile of this CTA: tiles are handed out in a static
 // round-robin over the CTAs.
@@ -177,11 +203,46 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& args, int t, int& m0
     n0 = nb * Cfg::BN;
 }
 
-template <class Cfg>
+// The t-th piece of work of this CTA: whole-tile mode, its t-th tile (chunks
+// 0 .. nc - 1); piece mode, the t-th tile its tail range touches, chunks
+// c0 .. c1 - 1 of it, and the piece's workspace slot (-1: the whole tile).
+template <class Cfg, bool SPLIT>
+__device__ __forceinline__ void piece_origin(const GemmArgs& args, int t, int& m0, int& n0, int& c0, int& c1,
+                                             int& slot)
+{
+    if constexpr (!SPLIT) {
+        tile_origin<Cfg>(args, t, m0, n0);
+        c0 = 0;
+        c1 = args.num_chunks;
+        slot = -1;
+    } else {
+        const int nc = args.num_chunks;
+        long long u0, u1;
+        tail_range(args.tail_units, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), u0, u1);
+        const int j = static_cast<int>(u0 / nc) + t;  // tile of the tail
+        const long long base = static_cast<long long>(j) * nc;
+        c0 = u0 > base ? static_cast<int>(u0 - base) : 0;
+        c1 = u1 - base < nc ? static_cast<int>(u1 - base) : nc;
+        slot = (c0 == 0 && c1 == nc) ? -1 : 2 * static_cast<int>(blockIdx.x) + (t == 0 ? 0 : 1);
+        const int id = args.tail_tile0 + j;
+        int mb, nb;
+        if (args.n_fastest) {
+            nb = id % args.tiles_n;
+            mb = id / args.tiles_n;
+        } else {
+            mb = id % args.tiles_m;
+            nb = id / args.tiles_m;
+        }
+        m0 = mb * Cfg::BM;
+        n0 = nb * Cfg::BN;
+    }
+}
+
+template <class Cfg, bool SPLIT = false>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     bfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmD,
-                     const GemmArgs args)
+                     const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,12 +266,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nc = args.num_chunks;
-    // tiles handed out round-robin over the CTAs
-    const int total_tiles = args.tiles_m * args.tiles_n;
+    // whole tiles handed out round-robin over the CTAs (whole-tile mode), or this
+    // CTA's range of the tail's chunks, in one or more pieces (piece mode)
     const int ncta = static_cast<int>(gridDim.x);
     const int cta = static_cast<int>(blockIdx.x);
-    const int my_tiles = total_tiles > cta ? (total_tiles - 1 - cta) / ncta + 1 : 0;
-    const int my_chunks = my_tiles * nc;
+    int my_tiles, my_chunks;
+    if constexpr (!SPLIT) {
+        const int total_tiles = args.tail_tile0;
+        my_tiles = total_tiles > cta ? (total_tiles - 1 - cta) / ncta + 1 : 0;
+        my_chunks = my_tiles * nc;
+    } else {
+        long long u0, u1;
+        tail_range(args.tail_units, cta, ncta, u0, u1);
+        my_chunks = static_cast<int>(u1 - u0);
+        my_tiles = u1 > u0 ? static_cast<int>((u1 - 1) / nc - u0 / nc) + 1 : 0;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -234,7 +304,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmSA);
         tma_prefetch_desc(&tmD);
+        if (SPLIT)
+            tma_prefetch_desc(&tmW);
     }
+    // The launch after this one on the stream, if it is a programmatic dependent
+    // (the piece-mode launch after the whole tiles; the tail reduce after the
+    // pieces), may be scheduled from now on.
+    grid_launch_dependents();
     if (warp == 1) {
         tmem_alloc<Cfg::TMEM_COLS>(tmem_slot);
         tmem_relinquish();
@@ -253,8 +329,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             int issued = 0;
-            int t = 0, c = 0, m0 = 0, n0 = 0;
-            tile_origin<Cfg>(args, 0, m0, n0);
+            int t = 0, c = 0, c_end = nc, m0 = 0, n0 = 0, slot;
+            piece_origin<Cfg, SPLIT>(args, 0, m0, n0, c, c_end, slot);
             // with the test switch on, nothing is loaded: the MMA issuer's first wait
             // runs out, and every role unwinds through its bounded waits
             const int to_issue = args.stall ? 0 : my_chunks;
@@ -274,10 +350,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tma_load_2d(sB + s * Cfg::B_BYTES, &tmB, &full[s], c * Cfg::BK, n0);
                 }
                 ++issued;
-                if (++c == nc) {
-                    c = 0;
+                if (++c == c_end) {
                     ++t;
-                    tile_origin<Cfg>(args, t, m0, n0);
+                    piece_origin<Cfg, SPLIT>(args, t, m0, n0, c, c_end, slot);
                 }
             }
             // make sure no copy is still landing in shared memory before exit: wait
@@ -289,17 +364,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == 2 || (Cfg::SCALE_WARPS == 2 && warp == 3)) {
         // ---------------------------------------------------------------- scale producer
         const int sp = warp - 2;  // this warp's share of the per-column scales
-        // Groups of SGROUP chunks of one tile (the last group of a tile may be
-        // shorter: TMA fills the rows past the last chunk with zeros, and the
-        // promotion warps never read them).
+        // Groups of SGROUP chunks of one tile, or of one piece in piece mode (the
+        // last group may be shorter: its rows past the end hold other chunks'
+        // scales, or TMA's zero fill past the last chunk, and the promotion warps
+        // never read them).
         constexpr int NSBS = Cfg::SGROUP * Cfg::SBS_PER_CHUNK;
         static_assert(NSBS <= 32, "one lane per scalar B scale of a group");
         int issued = 0;
         bool ok = true;
         for (int t = 0; t < my_tiles && ok; ++t) {
-            int m0, n0;
-            tile_origin<Cfg>(args, t, m0, n0);
-            for (int c0 = 0; c0 < nc; c0 += Cfg::SGROUP) {
+            int m0, n0, cb, ce, slot;
+            piece_origin<Cfg, SPLIT>(args, t, m0, n0, cb, ce, slot);
+            for (int c0 = cb; c0 < ce; c0 += Cfg::SGROUP) {
                 const int qs = issued % Cfg::SSTAGES;
                 const uint32_t qph = (issued / Cfg::SSTAGES) & 1;
                 // lane 0 waits and the warp follows its verdict, so that no lane can
@@ -436,8 +512,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int i = 0; i < CPW / 2; ++i)
             acc[i] = 0;
 
-        int t = 0, c = 0, m0 = 0, n0 = 0;
-        tile_origin<Cfg>(args, 0, m0, n0);
+        int t = 0, c = 0, c_end = nc, m0 = 0, n0 = 0, wslot = -1;
+        piece_origin<Cfg, SPLIT>(args, 0, m0, n0, c, c_end, wslot);
         int qs = 0, gi = 0;  // scale stage and chunk index within its group
         uint32_t qph = 0;
         for (int g = 0; g < my_chunks; ++g) {
@@ -549,7 +625,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
             // the group's last chunk (or the tile's): this warp is done with the stage
-            if (gi == Cfg::SGROUP - 1 || c == nc - 1) {
+            if (gi == Cfg::SGROUP - 1 || c == c_end - 1) {
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&sempty[qs]);
@@ -562,10 +638,61 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ++gi;
             }
 
-            if (++c == nc) {
+            if (++c == c_end) {
                 // ------------------------------------------------ BF16 epilogue of tile t
                 const int col0 = n0 + half * CPW;
-                if constexpr (Cfg::EPI == EPI_F32_ADD) {
+                bool f32_piece = false;  // a partial tile of piece mode: FP32 to the workspace
+                if constexpr (SPLIT)
+                    f32_piece = wslot >= 0;
+                if (f32_piece) {
+                    // FP32 boxes of 32 columns x 32 rows into the piece's workspace slot
+                    // (rows wslot * BM + ..., columns of the tile): the slab holds CPW/64
+                    // boxes, so the warp's CPW/32 boxes go out in two rounds.
+                    constexpr int SLAB = CPW / 64;
+                    const int y0 = wslot * Cfg::BM + quarter * 32;
+#pragma unroll
+                    for (int round = 0; round < 2; ++round) {
+                        if (lane == 0)
+                            tma_store_wait_read_all();  // earlier stores have read the slab
+                        __syncwarp();
+                        if constexpr (Cfg::SB_VEC) {
+                            // 16x256b layout (4 rows x G column pairs per thread)
+                            constexpr int G = Cfg::SBV_G;
+                            const int q4 = lane & 3, rs = lane >> 2;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int r = rs + 8 * k;
+#pragma unroll
+                                for (int gg = 0; gg < SLAB * 4; ++gg) {
+                                    const int chunk16 = 2 * (gg & 3) + (q4 >> 1);
+                                    *reinterpret_cast<uint64_t*>(my_out + (gg >> 2) * Cfg::BOX_BYTES + r * 128 +
+                                                                 ((chunk16 ^ (r & 7)) << 4) + 8 * (q4 & 1)) =
+                                        acc[k * G + round * SLAB * 4 + gg];
+                                }
+                            }
+                        } else {
+                            // 32x32b layout: the thread's row; box b holds pairs 16 b .. 16 b + 15
+#pragma unroll
+                            for (int bx = 0; bx < SLAB; ++bx) {
+                                const uint64_t* v = acc + (round * SLAB + bx) * 16;
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    *reinterpret_cast<ulonglong2*>(my_out + bx * Cfg::BOX_BYTES + lane * 128 +
+                                                                   ((q ^ (lane & 7)) << 4)) =
+                                        make_ulonglong2(v[2 * q], v[2 * q + 1]);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int bx = 0; bx < SLAB; ++bx)
+                                tma_store_2d(&tmW, my_out + bx * Cfg::BOX_BYTES, half * CPW + (round * SLAB + bx) * 32,
+                                             y0);
+                            tma_store_commit();
+                        }
+                    }
+                } else if constexpr (Cfg::EPI == EPI_F32_ADD) {
                     // FP32 boxes of 32 columns: the slab holds CPW/64 of them, so the
                     // CPW/32 boxes of the row go out in two rounds. The accumulators are
                     // in the 16x256b layout (4 rows x G column pairs per thread): each pair
@@ -649,9 +776,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < CPW / 2; ++i)
                     acc[i] = 0;
-                c = 0;
                 ++t;
-                tile_origin<Cfg>(args, t, m0, n0);
+                piece_origin<Cfg, SPLIT>(args, t, m0, n0, c, c_end, wslot);
             }
         }
         if (lane == 0)
@@ -663,6 +789,100 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<Cfg::TMEM_COLS>(tmem_base);
+    }
+    // piece mode runs beside the whole-tile launch before it; it completes only
+    // after that launch has, so that work after it on the stream finds every tile
+    if constexpr (SPLIT)
+        grid_dependency_wait();
+}
+
+// ---------------------------------------------------------------------------
+// The split tail tiles: tile j of the tail (tile tail_tile0 + j) was cut between
+// the CTAs whose ranges meet its chunk units j nc .. (j + 1) nc - 1; each wrote
+// its piece to its slot (2i for the CTA's first tail tile, 2i + 1 for its last).
+// This kernel adds the pieces in CTA order and stores the BF16 tile. A tile that
+// one CTA did whole was stored by that CTA and is skipped; CTAs between the
+// first and the last owner of a tile whose range is empty (possible when the
+// tail has fewer chunks than there are CTAs) wrote nothing and are skipped.
+// It is launched as a programmatic dependent of the piece-mode GEMM, so its
+// CTAs are staged while the GEMM finishes and start as soon as it has
+// completed. One CTA of 256 threads per 8 rows of a tail tile.
+struct TailReduceArgs {
+    const float* ws;
+    uint16_t* d;  // BF16 output
+    long long ldd;
+    int gm, gn, num_chunks, tail_tile0, grid;
+    long long tail_units;
+    int tiles_m, tiles_n, n_fastest;
+};
+
+// The CTA (of `grid`) whose tail range holds chunk unit u.
+__device__ __forceinline__ int tail_owner(long long u, long long units, int grid)
+{
+    return static_cast<int>(((u + 1) * grid - 1) / units);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(256) gemm_tail_reduce_kernel(const TailReduceArgs a)
+{
+    constexpr int BM = 128, ROWS = 8, VEC = 4, MAXP = 256;
+    __shared__ int slots[MAXP];
+    // launched as a programmatic dependent of the GEMM: wait until that grid has
+    // completed and its workspace stores are visible
+    grid_dependency_wait();
+    const int j = blockIdx.x;
+    const long long first = static_cast<long long>(j) * a.num_chunks;
+    const int i0 = tail_owner(first, a.tail_units, a.grid);
+    const int i1 = tail_owner(first + a.num_chunks - 1, a.tail_units, a.grid);
+    if (i0 == i1)
+        return;
+    // the tile's pieces in CTA order, one CTA per thread: slot of CTA i0 + t (2i for
+    // its first tail tile, 2i + 1 for its last), or -1 for a CTA with an empty range
+    const int np = i1 - i0 + 1;  // at most the grid size, which the host keeps <= MAXP
+    if (threadIdx.x < np) {
+        const int i = i0 + threadIdx.x;
+        long long s0, s1;
+        tail_range(a.tail_units, i, a.grid, s0, s1);
+        slots[threadIdx.x] = s0 == s1 ? -1 : 2 * i + (s0 / a.num_chunks == j ? 0 : 1);
+    }
+    __syncthreads();
+    const int id = a.tail_tile0 + j;
+    int mb, nb;
+    if (a.n_fastest) {
+        nb = id % a.tiles_n;
+        mb = id / a.tiles_n;
+    } else {
+        mb = id % a.tiles_m;
+        nb = id / a.tiles_m;
+    }
+    const int m0 = mb * BM, n0 = nb * BN;
+    for (int v = threadIdx.x; v < ROWS * BN / VEC; v += 256) {  // 4-column groups of this CTA's rows
+        const int r = blockIdx.y * ROWS + v / (BN / VEC), col = (v % (BN / VEC)) * VEC;
+        const float* base = a.ws + r * BN + col;
+        float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int p = 0; p < np; p += 4) {
+            // four pieces' loads in flight, added in order
+            float4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (p + u < np && slots[p + u] >= 0)
+                    q[u] = *reinterpret_cast<const float4*>(base + static_cast<long long>(slots[p + u]) * (BM * BN));
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (p + u < np && slots[p + u] >= 0) {
+                    sum.x += q[u].x;
+                    sum.y += q[u].y;
+                    sum.z += q[u].z;
+                    sum.w += q[u].w;
+                }
+        }
+        const int gr = m0 + r, gc = n0 + col;
+        if (gr < a.gm && gc < a.gn) {
+            uint2 o;
+            o.x = cvt_bf16x2(sum.x, sum.y);
+            o.y = cvt_bf16x2(sum.z, sum.w);
+            *reinterpret_cast<uint2*>(a.d + static_cast<long long>(gr) * a.ldd + gc) = o;
+        }
     }
 }
 

@@ -105,6 +105,20 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 }
 
 // 2-D tiled store of a shared-memory box to (x, y); out-of-range parts are dropped.
+// Programmatic dependent launch: let the grid launched after this one on the
+// stream (with the programmatic serialisation attribute) be scheduled now ...
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ... and, in that dependent grid, wait until the grids it depends on have
+// completed and their memory operations are visible (a no-op without them).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

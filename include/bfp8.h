@@ -95,23 +95,54 @@ int fp8_quantize_act_transpose(const void* x, int64_t R, int64_t C, int64_t ldx,
                                uint8_t* q, int64_t ldq, float* s, int64_t lds,
                                uint8_t* qt, int64_t ldqt, float* st, int64_t ldst, void* stream);
 
+/* Workspace of the three BF16 GEMMs below (fwd, dgrad, wgrad), all optional.
+ * The GEMMs run one persistent CTA per SM over 128-row output tiles. When the
+ * tiles do not fill the grid's last round, that partial round (the tail) can
+ * be split along the contraction axis: the whole rounds run in one launch; a
+ * second launch, which starts on the SMs that the first one frees, gives
+ * every CTA an equal contiguous share of the tail tiles' 128-wide chunks and
+ * writes pieces that are not a whole tile to the workspace as FP32 partial
+ * tiles; a third kernel adds the pieces of each tile in a fixed order and
+ * stores it in BF16 (all on `stream`). The tail then costs about (tail tiles / SMs) of a round instead of
+ * a whole round, and results stay deterministic (the same inputs give the
+ * same bits on every call); they differ from the unsplit GEMM's only in the
+ * FP32 summation order of the split tiles. The split is used when
+ * `workspace` is non-NULL, `workspace_bytes` is at least the size below, the
+ * tail leaves at least a quarter of the SMs idle, and splitting shortens the
+ * longest CTA's share of the tail by at least 40 chunks of 128 (below that,
+ * the extra launches and the partial tiles cost about what they save).
+ *   workspace: caller-owned device memory, 16-byte aligned, used as scratch
+ *   for the duration of the call (stream-ordered); calls that share one
+ *   workspace must be ordered on the device (one stream, or events).
+ *   NULL (or fewer bytes) = no split, the same results as before the split
+ *   existed, bit for bit.
+ * fp8_block_gemm_workspace_bytes: the size that enables the split on the
+ * current device (two FP32 partial tiles of 128 x 256 per SM: 37.9 MB on a
+ * 148-SM B300). */
+int fp8_block_gemm_workspace_bytes(int64_t* bytes);
+
 /* Forward GEMM, y = x W^T:
  *   y[m][n] = bf16( sum_kb sx[kb][m] * sw[n/128][kb] * sum_{k in kb} qx[m][k] qw[n][k] )
  *   qx [M][K] (ldqx), sx [K/128][M] (ldsx), qw [N][K] (ldqw), sw [N/128][K/128] dense,
  *   y [M][N] bf16 (ldy). K, N multiples of 128; M >= 0 any (M = 0 is a no-op).
- * Alignment: qx, qw, sx, y 16 B; ldqx, ldqw % 16 == 0; ldsx % 4 == 0; ldy % 8 == 0. */
+ *   workspace, workspace_bytes: see fp8_block_gemm_workspace_bytes (NULL, 0: none).
+ * Alignment: qx, qw, sx, y, workspace 16 B; ldqx, ldqw % 16 == 0; ldsx % 4 == 0;
+ * ldy % 8 == 0. */
 int fp8_block_gemm_fwd(const uint8_t* qx, int64_t ldqx, const float* sx, int64_t ldsx,
                        const uint8_t* qw, int64_t ldqw, const float* sw,
-                       void* y, int64_t ldy, int64_t M, int64_t N, int64_t K, void* stream);
+                       void* y, int64_t ldy, int64_t M, int64_t N, int64_t K,
+                       void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Input-gradient GEMM, dx = dy W (contraction over the layer's N outputs):
  *   dx[m][k] = bf16( sum_nb sdy[nb][m] * sw[nb][k/128] * sum_{n in nb} qdy[m][n] qw[n][k] )
  *   qdy [M][N] (ldqdy), sdy [N/128][M] (ldsdy), qw/sw exactly as produced for the
  *   forward pass (qw is read with the contraction axis strided), dx [M][K] bf16 (lddx).
+ *   workspace, workspace_bytes: as fp8_block_gemm_fwd.
  * Alignment: as fp8_block_gemm_fwd. */
 int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const float* sdy, int64_t ldsdy,
                          const uint8_t* qw, int64_t ldqw, const float* sw,
-                         void* dx, int64_t lddx, int64_t M, int64_t N, int64_t K, void* stream);
+                         void* dx, int64_t lddx, int64_t M, int64_t N, int64_t K,
+                         void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Weight-gradient GEMM, dW = dy^T x (contraction over the M tokens, padded
  * with zero codes to M128):
@@ -119,11 +150,13 @@ int fp8_block_gemm_dgrad(const uint8_t* qdy, int64_t ldqdy, const float* sdy, in
  *   qdyt [N][M128] (ldqdyt), sdyt [M128/128][N] (ldsdyt), qxt [K][M128] (ldqxt),
  *   sxt [M128/128][K] (ldsxt), all from fp8_quantize_transpose; dw [N][K] bf16 (lddw).
  *   M >= 1 any; N, K multiples of 128.
- * Alignment: qdyt, qxt, sdyt, sxt, dw 16 B; ldqdyt, ldqxt % 16 == 0;
+ *   workspace, workspace_bytes: as fp8_block_gemm_fwd.
+ * Alignment: qdyt, qxt, sdyt, sxt, dw, workspace 16 B; ldqdyt, ldqxt % 16 == 0;
  * ldsdyt, ldsxt % 4 == 0; lddw % 8 == 0. */
 int fp8_block_gemm_wgrad(const uint8_t* qdyt, int64_t ldqdyt, const float* sdyt, int64_t ldsdyt,
                          const uint8_t* qxt, int64_t ldqxt, const float* sxt, int64_t ldsxt,
-                         void* dw, int64_t lddw, int64_t M, int64_t N, int64_t K, void* stream);
+                         void* dw, int64_t lddw, int64_t M, int64_t N, int64_t K,
+                         void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Weight-gradient GEMM accumulated into an FP32 main gradient (the recipe
  * keeps training state in FP32; same article and section as above):
@@ -231,6 +264,12 @@ int bfp8_set_wait_limit_ns(int64_t ns);
  * Meant for tests of the error path only; on = 0 (default) restores normal
  * operation. Returns the previous setting (0 or 1), or BFP8_EINVAL. */
 int bfp8_test_stall_producers(int on);
+
+/* Number of kernels the library has launched in this process so far, on every
+ * device and stream (host-side count of successful launch calls; a call that
+ * is captured into a CUDA graph counts once, at capture). Returns BFP8_OK, or
+ * BFP8_EINVAL for a NULL pointer. */
+int bfp8_kernel_launches(int64_t* count);
 
 /* Tuning knob for the GEMMs' output tile width: 0 = automatic (default),
  * 128, 192 or 256 columns (192 applies to the forward and weight-gradient

@@ -25,7 +25,8 @@ def test_exports_every_declared_function(lib):
                           "fp8_block_gemm_fwd", "fp8_block_gemm_dgrad", "fp8_block_gemm_wgrad",
                           "fp8_block_gemm_wgrad_acc",
                           "bfp8_status_string", "bfp8_last_device_status", "bfp8_set_gemm_tile_n",
-                          "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers",
+                          "bfp8_set_wait_limit_ns", "bfp8_test_stall_producers", "bfp8_kernel_launches",
+                          "fp8_block_gemm_workspace_bytes",
                           "muonh_partials_len", "muonh_normalize", "muonh_apply", "muonh_apply_static",
                           "bf16_gemm_axpby", "muonh_newton_schulz_work_bytes", "muonh_newton_schulz"}
     cdll = ctypes.CDLL(bfp8.LIB_PATH)
@@ -43,6 +44,18 @@ def test_tile_knob(lib):
     assert lib.bfp8_set_gemm_tile_n(64) == EINVAL
     prev = lib.bfp8_set_gemm_tile_n(256)
     assert lib.bfp8_set_gemm_tile_n(prev) == 256
+
+
+def test_launch_counter(lib):
+    n = ctypes.c_int64(-1)
+    assert lib.bfp8_kernel_launches(None) == EINVAL
+    assert lib.bfp8_kernel_launches(ctypes.byref(n)) == OK
+    assert n.value >= 0
+    # calls refused on the host launch nothing
+    lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 130, 128, None, 0, None)
+    m = ctypes.c_int64(-1)
+    lib.bfp8_kernel_launches(ctypes.byref(m))
+    assert m.value == n.value
 
 
 def test_wait_limit_and_stall_switch_arguments(lib):
@@ -89,21 +102,27 @@ def test_quantiser_argument_checks(lib):
 def test_gemm_argument_checks(lib):
     s = None
     # fwd: N, K multiples of 128
-    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 130, 128, s) == ESHAPE
-    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 96, s) == ESHAPE
-    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 0, 128, 128, s) == OK
-    assert lib.fp8_block_gemm_fwd(None, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, s) == EINVAL
-    assert lib.fp8_block_gemm_fwd(A, 128, A, 3, A, 128, A, A, 128, 4, 128, 128, s) == EINVAL  # ldsx < M
-    assert lib.fp8_block_gemm_fwd(A, 128, A, 6, A, 128, A, A, 128, 6, 128, 128, s) == EALIGN  # ldsx % 4
-    assert lib.fp8_block_gemm_fwd(A, 136, A, 4, A, 136, A, A, 128, 4, 128, 128, s) == EALIGN  # ldq % 16
-    assert lib.fp8_block_gemm_fwd(A, 128, A + 4, 4, A, 128, A, A, 128, 4, 128, 128, s) == EALIGN
-    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 96, A, A, 96, 4, 128, 96, s) == ESHAPE
-    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 128, A, A, 100, 4, 128, 128, s) == EINVAL
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 130, 128, None, 0, s) == ESHAPE
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 96, None, 0, s) == ESHAPE
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 0, 128, 128, None, 0, s) == OK
+    assert lib.fp8_block_gemm_fwd(None, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, None, 0, s) == EINVAL
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 3, A, 128, A, A, 128, 4, 128, 128, None, 0, s) == EINVAL  # ldsx < M
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 6, A, 128, A, A, 128, 6, 128, 128, None, 0, s) == EALIGN  # ldsx % 4
+    assert lib.fp8_block_gemm_fwd(A, 136, A, 4, A, 136, A, A, 128, 4, 128, 128, None, 0, s) == EALIGN  # ldq % 16
+    assert lib.fp8_block_gemm_fwd(A, 128, A + 4, 4, A, 128, A, A, 128, 4, 128, 128, None, 0, s) == EALIGN
+    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 96, A, A, 96, 4, 128, 96, None, 0, s) == ESHAPE
+    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 128, A, A, 100, 4, 128, 128, None, 0, s) == EINVAL
     # wgrad: M >= 1, ld of transposed codes >= M128
-    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 0, 128, 128, s) == ESHAPE
-    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 200, 128, 128, s) == EINVAL
-    assert lib.fp8_block_gemm_wgrad(A, 256, A, 126, A, 256, A, 128, A, 128, 200, 128, 128, s) == EINVAL
-    assert lib.fp8_block_gemm_wgrad(A, 256, A, 130, A, 256, A, 128, A, 128, 200, 128, 128, s) == EALIGN
+    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 0, 128, 128, None, 0, s) == ESHAPE
+    assert lib.fp8_block_gemm_wgrad(A, 128, A, 128, A, 128, A, 128, A, 128, 200, 128, 128, None, 0, s) == EINVAL
+    assert lib.fp8_block_gemm_wgrad(A, 256, A, 126, A, 256, A, 128, A, 128, 200, 128, 128, None, 0, s) == EINVAL
+    assert lib.fp8_block_gemm_wgrad(A, 256, A, 130, A, 256, A, 128, A, 128, 200, 128, 128, None, 0, s) == EALIGN
+    # the optional workspace: a negative size or a misaligned pointer is refused
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, A, -1, s) == EINVAL
+    assert lib.fp8_block_gemm_fwd(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, A + 8, 1 << 20, s) == EALIGN
+    assert lib.fp8_block_gemm_dgrad(A, 128, A, 4, A, 128, A, A, 128, 4, 128, 128, A + 4, 1 << 20, s) == EALIGN
+    assert lib.fp8_block_gemm_wgrad(A, 256, A, 128, A, 256, A, 128, A, 128, 200, 128, 128, A, -5, s) == EINVAL
+    assert lib.fp8_block_gemm_workspace_bytes(None) == EINVAL
     # wgrad accumulating into FP32: same operand rules, FP32 main gradient with ldmg % 4 == 0
     acc = lib.fp8_block_gemm_wgrad_acc
     assert acc(A, 128, A, 128, A, 128, A, 128, A, 128, 0, 128, 128, s) == ESHAPE
