@@ -433,6 +433,42 @@ int run_quant_dual(const void* x, int64_t R, int64_t C, int64_t ldx, const Quant
     return launch_status();
 }
 
+// Launches the weight quantiser (quant_weight_kernel): the same buffers and CTAs per
+// SM as the two-layout kernel.
+int run_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, const QuantArgs& base, cudaStream_t stream)
+{
+    int dev = 0;
+    int rc = check_arch(&dev);
+    if (rc != BFP8_OK)
+        return rc;
+    unsigned* status = device_status_ptr(dev);
+    if (!status)
+        return BFP8_ELAUNCH;
+    CUtensorMap tm;
+    if (!make_map(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                  static_cast<uint64_t>(ldw) * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return BFP8_ELAUNCH;
+    constexpr int smem = dual_smem_bytes<kDualBuffers>();
+    static std::atomic<bool> attr_set[kMaxDevices];
+    auto kern = quant_weight_kernel<kDualBuffers, kDualCtasPerSm>;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return BFP8_ELAUNCH;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    QuantArgs a = base;
+    a.R = N;
+    a.nblk_c = K / 128;
+    a.nblocks = (N / 128) * a.nblk_c;
+    a.status = status;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    a.stall = g_stall.load(std::memory_order_relaxed);
+    const int64_t ctas = std::min<int64_t>(a.nblocks, static_cast<int64_t>(sm_count(dev)) * kDualCtasPerSm);
+    kern<<<static_cast<unsigned>(ctas), kDualThreads, smem, stream>>>(tm, a);
+    note_launch();
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace bfp8
 
@@ -482,7 +518,7 @@ extern "C" int fp8_quantize_weight(const void* w, int64_t N, int64_t K, int64_t 
     qa.ldq = ldq;
     qa.s = s;
     qa.lds = K / 128;
-    return run_quant_blocks<MODE_WEIGHT>(w, N, K, ldw, qa, static_cast<cudaStream_t>(stream));
+    return run_quant_weight(w, N, K, ldw, qa, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quantize_transpose(const void* x, int64_t R, int64_t C, int64_t ldx, uint8_t* qt,

@@ -105,6 +105,23 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 }
 
 // 2-D tiled store of a shared-memory box to (x, y); out-of-range parts are dropped.
+// Named-barrier AND vote of `nthreads` threads (a multiple of 32) on barrier `id`:
+// every participant gets the AND of all participants' `v`, and the barrier orders
+// their shared-memory accesses like bar.sync.
+__device__ __forceinline__ bool bar_red_and(int id, int nthreads, bool v)
+{
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1 : 0), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Programmatic dependent launch: let the grid launched after this one on the
 // stream (with the programmatic serialisation attribute) be scheduled now ...
 __device__ __forceinline__ void grid_launch_dependents()

@@ -307,10 +307,9 @@ __device__ __forceinline__ void column_pass(const uint32_t (*tile)[64], uint32_t
 // encode the current one, so HBM reads overlap the arithmetic.
 //   MODE_ROWS:   1x128 tiles along the columns -> q [R][C], s [C/128][R]
 //   MODE_COLS:   1x128 tiles down the rows     -> qt [C][R128], st [R128/128][C]
-//   MODE_WEIGHT: one 128x128 block per scale   -> q [R][C], s [R/128][C/128]
 // (both activation layouts from one read: quant_dual_kernel below)
 // ---------------------------------------------------------------------------
-enum QuantMode { MODE_ROWS = 1, MODE_COLS = 2, MODE_WEIGHT = 4 };
+enum QuantMode { MODE_ROWS = 1, MODE_COLS = 2 };
 
 struct QuantArgs {
     int64_t R, nblk_c, nblocks;
@@ -401,22 +400,29 @@ __device__ __forceinline__ void store_codes32(uint8_t* dst, const uint32_t (&c)[
 // With ST32 every column's 32 codes go out as one 32-byte store (qt and ldqt 32-byte
 // aligned), else as two 16-byte stores.
 template <bool ST32>
-__device__ __forceinline__ void column_pass_4w(const uint32_t (*tile)[64], uint32_t (*part)[64], const ScaleTables& tab,
-                                               int64_t cb, int64_t rb, uint8_t* __restrict__ qt, int64_t ldqt,
-                                               float* __restrict__ st, int64_t ldst)
+__device__ __forceinline__ bool column_pass_4w(bool ok, const uint32_t (*tile)[64], uint32_t (*part)[64],
+                                               const ScaleTables& tab, int64_t cb, int64_t rb,
+                                               uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ st,
+                                               int64_t ldst)
 {
     const int t = threadIdx.x - 128;
     const int w = t >> 5, lane = t & 31;
     const int half = w >> 1;
     const int cw = (w & 1) * 32 + lane;
     const int col = 2 * cw;
-    uint32_t m = 0;
+    if (ok) {
+        uint32_t m = 0;
 #pragma unroll 16
-    for (int i = 0; i < 64; ++i)
-        m = bf16x2_maxabs(m, tile[half * 64 + i][cw]);
-    part[half][cw] = m & 0x7FFF7FFFu;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    m = bf16x2_max(part[0][cw], part[1][cw]);
+        for (int i = 0; i < 64; ++i)
+            m = bf16x2_maxabs(m, tile[half * 64 + i][cw]);
+        part[half][cw] = m & 0x7FFF7FFFu;
+    }
+    // the four warps combine their halves here, and take one decision on whether the
+    // block's copy arrived (a warp whose wait gave up reads nothing and votes no), so
+    // that none of them can be left waiting at this barrier for the others
+    if (!bar_red_and(1, 128, ok))
+        return false;
+    const uint32_t m = bf16x2_max(part[0][cw], part[1][cw]);
     const TileScale s0 = tile_scale_tab(bf16_lo(m), tab), s1 = tile_scale_tab(bf16_hi(m), tab);
     const PairScale ps = pair_scale(s0, s1);
     uint8_t* out0 = qt + (cb * 128 + col) * ldqt + rb * 128 + half * 64;
@@ -440,6 +446,7 @@ __device__ __forceinline__ void column_pass_4w(const uint32_t (*tile)[64], uint3
     }
     if (half == 0)
         *reinterpret_cast<float2*>(st + rb * ldst + cb * 128 + col) = make_float2(s0.s, s1.s);
+    return true;
 }
 
 constexpr int kQuantTileBytes = 128 * 128 * 2;
@@ -452,11 +459,9 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[2];
     __shared__ __align__(16) uint32_t part[4][64];
-    __shared__ uint32_t red[8];
     __shared__ ScaleTables stab;
     __shared__ int abort_flag;
     const int tid = threadIdx.x;
-    const int sub = tid & 15;
 
     const int64_t first = blockIdx.x;
     const int64_t stride = gridDim.x;
@@ -504,39 +509,6 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
         }
         if (MODE == MODE_COLS)
             column_pass(tile, part, stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
-        if (MODE == MODE_WEIGHT) {
-            uint32_t m = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                m = bf16x2_max(m, absmax_pairs(*reinterpret_cast<const uint4*>(&tile[(tid >> 4) + 16 * j][sub * 4])));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if ((tid & 31) == 0)
-                red[tid >> 5] = m;
-            __syncthreads();
-            m = red[0];
-#pragma unroll
-            for (int k = 1; k < 8; ++k)
-                m = bf16x2_max(m, red[k]);
-            const TileScale ts = tile_scale_tab(fmaxf(bf16_lo(m), bf16_hi(m)), stab);
-            const PairScale ps = pair_scale(ts, ts);
-            auto encode = [&](auto scaled) {
-#pragma unroll 2
-                for (int j = 0; j < 8; ++j) {
-                    const int row = (tid >> 4) + 16 * j;
-                    const uint4 v = *reinterpret_cast<const uint4*>(&tile[row][sub * 4]);
-                    *reinterpret_cast<uint2*>(a.q + (rb * 128 + row) * a.ldq + cb * 128 + sub * 8) =
-                        codes8_packed<decltype(scaled)::value>(v, ps);
-                }
-            };
-            if (ps.scaled)
-                encode(std::true_type{});
-            else
-                encode(std::false_type{});
-            if (tid == 0)
-                a.s[rb * a.lds + cb] = ts.s;
-        }
         __syncthreads();  // everyone is done with this buffer (and with part / red)
         if (tid == 0 && i + 2 < my_blocks)
             issue(i + 2);
@@ -563,6 +535,37 @@ __global__ void __launch_bounds__(256, 3) quant_blocks_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 constexpr int kDualWorkers = 8;
 constexpr int kDualThreads = 32 * (kDualWorkers + 1);
+
+// The producer warp of the barrier-free block kernels: lane 0 loads this CTA's
+// blocks (first = blockIdx.x, stride = gridDim.x) into NB buffers, each refilled
+// once all kDualWorkers worker warps have arrived on its "empty" barrier.
+template <int NB>
+__device__ __forceinline__ void block_producer(const CUtensorMap& tmX, const QuantArgs& a, uint8_t* tiles,
+                                               uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                               int my_blocks)
+{
+    if ((threadIdx.x & 31) != 0)
+        return;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    int issued = 0;
+    const int to_issue = a.stall ? 0 : my_blocks;
+    for (int i = 0; i < to_issue; ++i) {
+        const int b = i % NB;
+        // the buffer's previous block (i - NB) has been consumed by every worker
+        if (i >= NB && !mbar_wait(&empty[b], ((i / NB) - 1) & 1, abort_flag, a.status, a.wait_ns))
+            break;
+        const int64_t blk = first + static_cast<int64_t>(i) * stride;
+        const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
+        mbar_arrive_expect_tx(&full[b], kQuantTileBytes);
+        tma_load_2d(tiles + b * kQuantTileBytes, &tmX, &full[b], static_cast<int32_t>(cb * 128),
+                    static_cast<int32_t>(rb * 128));
+        ++issued;
+    }
+    // no copy may still be landing in shared memory at exit
+    volatile int never = 0;
+    for (int i = issued - NB < 0 ? 0 : issued - NB; i < issued; ++i)
+        mbar_wait(&full[i % NB], (i / NB) & 1, &never, a.status, a.wait_ns);
+}
 
 template <int NB>
 constexpr int dual_smem_bytes()
@@ -601,27 +604,7 @@ __global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
     __syncthreads();
 
     if (warp == kDualWorkers) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            int issued = 0;
-            const int to_issue = a.stall ? 0 : my_blocks;
-            for (int i = 0; i < to_issue; ++i) {
-                const int b = i % NB;
-                // the buffer's previous block (i - NB) has been consumed by every worker
-                if (i >= NB && !mbar_wait(&empty[b], ((i / NB) - 1) & 1, &abort_flag, a.status, a.wait_ns))
-                    break;
-                const int64_t blk = first + static_cast<int64_t>(i) * stride;
-                const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
-                mbar_arrive_expect_tx(&full[b], kQuantTileBytes);
-                tma_load_2d(tiles + b * kQuantTileBytes, &tmX, &full[b], static_cast<int32_t>(cb * 128),
-                            static_cast<int32_t>(rb * 128));
-                ++issued;
-            }
-            // no copy may still be landing in shared memory at exit
-            volatile int never = 0;
-            for (int i = issued - NB < 0 ? 0 : issued - NB; i < issued; ++i)
-                mbar_wait(&full[i % NB], (i / NB) & 1, &never, a.status, a.wait_ns);
-        }
+        block_producer<NB>(tmX, a, tiles, full, empty, &abort_flag, my_blocks);
         return;
     }
 
@@ -629,19 +612,116 @@ __global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
         const int b = i % NB;
         const int64_t blk = first + static_cast<int64_t>(i) * stride;
         const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
-        // every worker waits on the same phase, so all of them give up together
-        if (!mbar_wait(&full[b], (i / NB) & 1, &abort_flag, a.status, a.wait_ns))
-            break;
+        // every worker waits on the same phase; a wait that gives up sets the abort
+        // flag, which ends the others' waits too
+        const bool ok = mbar_wait(&full[b], (i / NB) & 1, &abort_flag, a.status, a.wait_ns);
         const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + b * kQuantTileBytes);
         if (warp < 4) {
+            if (!ok)
+                break;
             row_tiles8(tile, stab, a, rb, cb, tid >> 4, 8);
             row_tiles8(tile, stab, a, rb, cb, (tid >> 4) + 64, 8);
-        } else {
-            column_pass_4w<ST32>(tile, part[i & 1], stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst);
+        } else if (!column_pass_4w<ST32>(ok, tile, part[i & 1], stab, cb, rb, a.qt, a.ldqt, a.st, a.ldst)) {
+            break;
         }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&empty[b]);
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Weight blocks (128x128, one scale per block) without block-wide barriers on
+// the copies: a producer warp (warp 8) keeps NB buffers in flight with full and
+// empty mbarriers, as in quant_dual_kernel. Each of the eight worker warps reads
+// 16 rows of the block into registers (rows r0 + 16 j, 8 columns per thread),
+// hands the buffer back, and votes on one 256-thread named barrier that also
+// combines the warps' maxima (scratch indexed by the block's parity, so a fast
+// warp can write the next block's maximum while a slow one still reads this
+// block's); then it encodes its 16 rows from the registers.
+// ---------------------------------------------------------------------------
+template <int NB, int MIN_CTAS>
+__global__ void __launch_bounds__(kDualThreads, MIN_CTAS)
+    quant_weight_kernel(const __grid_constant__ CUtensorMap tmX, const QuantArgs a)
+{
+    extern __shared__ uint8_t qsmem_raw[];
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsmem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[NB];
+    __shared__ __align__(8) uint64_t empty[NB];
+    __shared__ uint32_t red[2][kDualWorkers];
+    __shared__ ScaleTables stab;
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int my_blocks = a.nblocks > first ? static_cast<int>((a.nblocks - 1 - first) / stride + 1) : 0;
+
+    init_scale_tables(stab);
+    if (tid == 0) {
+        for (int b = 0; b < NB; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], kDualWorkers);
+        }
+        abort_flag = 0;
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tmX);
+    }
+    __syncthreads();
+
+    if (warp == kDualWorkers) {
+        block_producer<NB>(tmX, a, tiles, full, empty, &abort_flag, my_blocks);
+        return;
+    }
+
+    const int sub = tid & 15, r0 = tid >> 4;  // rows r0 + 16 j, columns 8 sub .. 8 sub + 7
+    for (int i = 0; i < my_blocks; ++i) {
+        const int b = i % NB;
+        const int64_t blk = first + static_cast<int64_t>(i) * stride;
+        const int64_t rb = blk / a.nblk_c, cb = blk - rb * a.nblk_c;
+        const bool ok = mbar_wait(&full[b], (i / NB) & 1, &abort_flag, a.status, a.wait_ns);
+        const uint32_t(*tile)[64] = reinterpret_cast<const uint32_t(*)[64]>(tiles + b * kQuantTileBytes);
+        uint4 v[8];
+        if (ok) {
+            uint32_t m = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[j] = *reinterpret_cast<const uint4*>(&tile[r0 + 16 * j][sub * 4]);
+                m = bf16x2_max(m, absmax_pairs(v[j]));
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                m = bf16x2_max(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0)
+                red[i & 1][warp] = m;
+        }
+        // one decision for all workers on whether the copy arrived, and the warps' maxima
+        if (!bar_red_and(1, 32 * kDualWorkers, ok))
+            break;
+        // the block is in registers: the buffer can be refilled while it is encoded
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[b]);
+        uint32_t m = red[i & 1][0];
+#pragma unroll
+        for (int k = 1; k < kDualWorkers; ++k)
+            m = bf16x2_max(m, red[i & 1][k]);
+        const TileScale ts = tile_scale_tab(fmaxf(bf16_lo(m), bf16_hi(m)), stab);
+        const PairScale ps = pair_scale(ts, ts);
+        uint8_t* out = a.q + (rb * 128 + r0) * a.ldq + cb * 128 + sub * 8;
+        auto encode = [&](auto scaled) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint2*>(out + 16 * j * a.ldq) = codes8_packed<decltype(scaled)::value>(v[j], ps);
+        };
+        if (ps.scaled)
+            encode(std::true_type{});
+        else
+            encode(std::false_type{});
+        if (tid == 0)
+            a.s[rb * a.lds + cb] = ts.s;
     }
 }
 
