@@ -307,3 +307,18 @@ def test_small_shapes_with_split_tail(tile_n, workspace, M, N, K, Mw):
     qxt[:, Mw:] = 0
     sdyt, sxt = wl.random_scales((M128 // TILE, N), 71), wl.random_scales((M128 // TILE, 384), 72)
     _check(*run_wgrad(qdyt, sdyt, qxt, sxt, Mw, ws=workspace), "wgrad")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 8192), (3, 640, 6144)])
+def test_split_tail_with_a_single_row_tile(workspace, M, N, K):
+    """A handful of output rows and a long contraction: one or three tiles, each cut into one-chunk
+    pieces over 64-144 CTAs; the partial tiles' rows past M are zero and must not be written."""
+    qx, sx = wl.random_codes((M, K), 95), wl.random_scales((K // TILE, M), 96)
+    qw, sw = wl.random_codes((N, K), 97), wl.random_scales((N // TILE, K // TILE), 98)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _expect_split(-(-N // 256), K // TILE, sms)
+    buf, y = _guarded(M, N)
+    bfp8.fp8_block_gemm_fwd(to_dev(qx), scales_to_dev(sx), to_dev(qw), to_dev(sw), y, workspace=workspace)
+    torch.cuda.synchronize()
+    assert _untouched(buf, M, N)
+    _check(from_dev_bf16(y), oracle.gemm_fwd(qx, sx, qw, sw), "fwd, split single row tile")
