@@ -24,12 +24,17 @@
 // subnormal scales) work on a and s both multiplied by 2^64, which changes
 // neither the quotient nor any rounding. The steps are odd in a (every
 // rounding is to nearest-even), so the quotient of a signed x carries x's
-// sign, except that an exact zero comes out as +0: x's sign bit is therefore
-// OR-ed into the code afterwards, which keeps -0 (and negative quotients that
-// round to zero) as 0x80. An all-zero tile (s = 0) runs the same instructions
-// with y = 0 and yields the inputs' signed zeros. Where a is so small against
-// s that a remainder still underflows, the quotient is below 2^-40 and its
-// code is a signed zero either way.
+// sign. They run on -x and -y, with the remainder's sign flipped:
+//   q0 = (-x)(-y),  r' = fma(q, s, -x) = -(x - q s),  q = fma(r', -y, q),
+// which gives the same values as the textbook form but keeps the sign of a
+// zero: for x = -0 the remainder is +0 and q = (+0)(-y) + (-0) = -0, where the
+// textbook fma(r, y, q) would give +0. So q = RN(x / s) bit for bit, signed
+// zeros included, and the E4M3 conversion (which keeps the sign of values that
+// round to zero) gives 0x80 for -0 and for negative quotients below the
+// smallest code. An all-zero tile (s = 0) runs the same instructions with y = 0
+// and yields the inputs' signed zeros. Where a is so small against s that a
+// remainder still underflows, the quotient is below 2^-40 and its code is a
+// signed zero either way.
 //
 // All four kernels are HBM-bound (2 B read + 1 B written per element and per
 // code layout): reads are 16-byte vector loads that cover whole 128-byte lines,
@@ -113,20 +118,20 @@ __device__ __forceinline__ TileScale tile_scale_tab(float amax, const ScaleTable
 // which take a separate code path). Lane i of every operand belongs to value i.
 // ---------------------------------------------------------------------------
 struct PairScale {
-    uint64_t ns;   // {-sp_lo, -sp_hi}
-    uint64_t y;    // {y_lo, y_hi}
+    uint64_t sp;   // {sp_lo, sp_hi}
+    uint64_t ny;   // {-y_lo, -y_hi}
     uint64_t pre;  // {pre_lo, pre_hi}
     bool scaled;   // some lane has pre != 1
 };
 
 // One scale for both lanes, from a broadcast (y, signed sp): sp > 0 marks a
-// pre-scaled tile, and the FMA operand is -|sp| either way.
+// pre-scaled tile, and the FMA operand is |sp| either way.
 __device__ __forceinline__ PairScale pair_scale_bcast(float y, float sp_signed)
 {
     PairScale p;
-    const float ns = -fabsf(sp_signed);
-    p.ns = pack_f32x2(ns, ns);
-    p.y = pack_f32x2(y, y);
+    const float sp = fabsf(sp_signed);
+    p.sp = pack_f32x2(sp, sp);
+    p.ny = pack_f32x2(-y, -y);
     p.pre = pack_f32x2(0x1p64f, 0x1p64f);
     p.scaled = sp_signed > 0.0f;
     return p;
@@ -135,33 +140,33 @@ __device__ __forceinline__ PairScale pair_scale_bcast(float y, float sp_signed)
 __device__ __forceinline__ PairScale pair_scale(const TileScale& lo, const TileScale& hi)
 {
     PairScale p;
-    p.ns = pack_f32x2(-lo.sp, -hi.sp);
-    p.y = pack_f32x2(lo.y, hi.y);
+    p.sp = pack_f32x2(lo.sp, hi.sp);
+    p.ny = pack_f32x2(-lo.y, -hi.y);
     p.pre = pack_f32x2(lo.pre, hi.pre);
     p.scaled = lo.pre != 1.0f || hi.pre != 1.0f;
     return p;
 }
 
-// a packed BF16 pair as a packed FP32 pair (exact)
-__device__ __forceinline__ uint64_t unpack2(uint32_t w)
+// a packed BF16 pair as a packed FP32 pair, negated (exact; -0 for +0)
+__device__ __forceinline__ uint64_t unpack2_neg(uint32_t w)
 {
-    return pack_f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return pack_f32x2(__uint_as_float((w << 16) ^ 0x80000000u), __uint_as_float((w & 0xFFFF0000u) ^ 0x80000000u));
 }
 
-// RN(a / s) lane-wise for a packed pair (SCALED: the tile pair has a 2^64
-// pre-scaling factor; the kernels branch on PairScale::scaled)
+// RN(a / s) lane-wise for a packed pair, from na = -a (SCALED: the tile pair has
+// a 2^64 pre-scaling factor; the kernels branch on PairScale::scaled)
 template <bool SCALED>
-__device__ __forceinline__ uint64_t quotient2(uint64_t a, const PairScale& ps)
+__device__ __forceinline__ uint64_t quotient2(uint64_t na, const PairScale& ps)
 {
     if (SCALED)
-        a = fmul2(a, ps.pre);
-    uint64_t q = fmul2(a, ps.y);
-    uint64_t r = a;
-    ffma2(r, q, ps.ns);  // r = a - q s
-    ffma2(q, r, ps.y);   // q = q + r y
-    r = a;
-    ffma2(r, q, ps.ns);
-    ffma2(q, r, ps.y);
+        na = fmul2(na, ps.pre);
+    uint64_t q = fmul2(na, ps.ny);  // q = a y
+    uint64_t r = na;
+    ffma2(r, q, ps.sp);  // r' = q s - a
+    ffma2(q, r, ps.ny);  // q = q - r' y = q + (a - q s) y
+    r = na;
+    ffma2(r, q, ps.sp);
+    ffma2(q, r, ps.ny);
     return q;
 }
 
@@ -191,13 +196,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(uint64_t q01, uint64_t q23)
     return r;
 }
 
-// Sign bits of two BF16 pair words, placed as the sign bits of the four codes
-// that cvt_e4m3x4 makes of them (bit 7 of bytes 1 and 3 of each word)
-__device__ __forceinline__ uint32_t sign_bits4(uint32_t w01, uint32_t w23)
-{
-    return __byte_perm(w01, w23, 0x7531) & 0x80808080u;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
 {
     uint32_t d;
@@ -224,9 +222,11 @@ __device__ __forceinline__ uint32_t absmax_pairs(const uint4& v)
 template <bool SCALED>
 __device__ __forceinline__ uint2 codes8_packed(const uint4& v, const PairScale& ps)
 {
-    const uint32_t lo = cvt_e4m3x4(quotient2<SCALED>(unpack2(v.x), ps), quotient2<SCALED>(unpack2(v.y), ps));
-    const uint32_t hi = cvt_e4m3x4(quotient2<SCALED>(unpack2(v.z), ps), quotient2<SCALED>(unpack2(v.w), ps));
-    return make_uint2(lo | sign_bits4(v.x, v.y), hi | sign_bits4(v.z, v.w));
+    const uint32_t lo =
+        cvt_e4m3x4(quotient2<SCALED>(unpack2_neg(v.x), ps), quotient2<SCALED>(unpack2_neg(v.y), ps));
+    const uint32_t hi =
+        cvt_e4m3x4(quotient2<SCALED>(unpack2_neg(v.z), ps), quotient2<SCALED>(unpack2_neg(v.w), ps));
+    return make_uint2(lo, hi);
 }
 
 __device__ __forceinline__ uint2 codes8(const uint4& v, const PairScale& ps)
@@ -254,10 +254,10 @@ __device__ __forceinline__ void column_encode(const uint32_t (*tile)[64], int qu
     for (int j = 0; j < 8; ++j) {
         const int r = quarter * 32 + 4 * j;
         const uint32_t w0 = tile[r][cw], w1 = tile[r + 1][cw], w2 = tile[r + 2][cw], w3 = tile[r + 3][cw];
-        const uint32_t a = cvt_e4m3x4(quotient2<SCALED>(unpack2(w0), ps), quotient2<SCALED>(unpack2(w1), ps)) |
-                           sign_bits4(w0, w1);
-        const uint32_t b = cvt_e4m3x4(quotient2<SCALED>(unpack2(w2), ps), quotient2<SCALED>(unpack2(w3), ps)) |
-                           sign_bits4(w2, w3);
+        const uint32_t a =
+            cvt_e4m3x4(quotient2<SCALED>(unpack2_neg(w0), ps), quotient2<SCALED>(unpack2_neg(w1), ps));
+        const uint32_t b =
+            cvt_e4m3x4(quotient2<SCALED>(unpack2_neg(w2), ps), quotient2<SCALED>(unpack2_neg(w3), ps));
         c0[j] = __byte_perm(a, b, 0x6420);
         c1[j] = __byte_perm(a, b, 0x7531);
     }

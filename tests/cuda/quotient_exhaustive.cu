@@ -47,10 +47,10 @@ __global__ void check(unsigned long long* pairs, unsigned long long* bad, unsign
         if ((xb2 & 0x7FFFu) > ab)
             xb2 &= 0x8000u;
         const uint32_t w = xb | (xb2 << 16);
-        // the kernels' sequence: signed quotient, codes, then the inputs' sign bits OR-ed in
-        const uint64_t a = bfp8::unpack2(w);
-        const uint64_t q = ps.scaled ? bfp8::quotient2<true>(a, ps) : bfp8::quotient2<false>(a, ps);
-        const uint32_t code = bfp8::cvt_e4m3x4(q, 0) | bfp8::sign_bits4(w, 0u);
+        // the kernels' sequence: the negated pair, the signed quotient, its codes
+        const uint64_t na = bfp8::unpack2_neg(w);
+        const uint64_t q = ps.scaled ? bfp8::quotient2<true>(na, ps) : bfp8::quotient2<false>(na, ps);
+        const uint32_t code = bfp8::cvt_e4m3x4(q, 0);
         const unsigned vals[2] = {xb, xb2};
 #pragma unroll
         for (int lane = 0; lane < 2; ++lane) {
