@@ -44,9 +44,10 @@
 //   warps 4..   promotion (8 warps; 12 with 192-wide tiles): warp w owns
 //               TMEM lanes 32 (w%4) .. +31 (output rows) and BN/(PW/4)
 //               columns; per chunk it reads the partial sums with tcgen05.ld
-//               in quarters of 32 columns (later quarters loading while earlier
-//               ones are promoted), releases the TMEM buffer once its last
-//               quarter has landed, and accumulates
+//               (scalar B scales: 32x32b, in quarters of 32 columns, later
+//               quarters loading while earlier ones are promoted; per-column B
+//               scales: 16x256b, in two 64-column blocks), releases the TMEM
+//               buffer once its last load has landed, and accumulates
 //               acc += partial * (sA * sB)  in FP32
 //               registers with packed two-lane FP32 instructions (scalar FP32
 //               instructions issued at this rate halve the tensor core's MMA
@@ -59,7 +60,7 @@
 //               and has the TMA unit add it into an FP32 D (D += acc).
 // With BN = 256 the promotion warps need more than the 168 registers a
 // 384-thread CTA gets; setmaxnreg moves registers from the producer/MMA
-// warpgroup to the promotion warpgroups (56/224, or 64/216 with per-column
+// warpgroup to the promotion warpgroups (56/224, or 40/232 with per-column
 // B scales), within the launch budget of 384 x 168 (12 promotion warps at
 // BN = 192: 56/152 within 512 x 128).
 // Every mbarrier wait is bounded (mbar_wait); a timeout sets the library's

@@ -36,10 +36,10 @@
 // remainder still underflows, the quotient is below 2^-40 and its code is a
 // signed zero either way.
 //
-// All four kernels are HBM-bound (2 B read + 1 B written per element and per
-// code layout): reads are 16-byte vector loads that cover whole 128-byte lines,
-// amax reductions use warp shuffles (or a shared-memory column pass for the
-// transposed layout).
+// The kernels are meant to be HBM-bound (2 B read + 1 B written per element and
+// per code layout): blocks arrive by TMA, shared-memory reads are 16-byte vector
+// loads (4-byte column reads for the transposed layout), amax reductions use warp
+// shuffles and a shared-memory combine across warps.
 #pragma once
 
 #include <cstdint>
@@ -396,7 +396,8 @@ __device__ __forceinline__ void store_codes32(uint8_t* dst, const uint32_t (&c)[
 // quant_dual_kernel): thread
 // t' = t - 128 takes the column pair 32 ((t'/32) % 2) + lane over rows
 // 64 (t'/64) .. +63; the two row halves combine their amax through shared
-// memory behind a barrier of these 128 threads only.
+// memory behind a barrier of these 128 threads only, which is also their vote
+// on whether the block's copy arrived.
 // With ST32 every column's 32 codes go out as one 32-byte store (qt and ldqt 32-byte
 // aligned), else as two 16-byte stores.
 template <bool ST32>
