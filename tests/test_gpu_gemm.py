@@ -322,3 +322,34 @@ def test_split_tail_with_a_single_row_tile(workspace, M, N, K):
     torch.cuda.synchronize()
     assert _untouched(buf, M, N)
     _check(from_dev_bf16(y), oracle.gemm_fwd(qx, sx, qw, sw), "fwd, split single row tile")
+
+
+def test_split_gemm_replays_from_a_cuda_graph(workspace):
+    """The split launches (whole rounds, pieces as a programmatic dependent, tail reduce) captured in
+    a CUDA graph replay to the eager call's bits, also after new operands are copied in."""
+    M, N, K = 8192, 2048, 12288  # 512 output tiles, 96 chunks: the rounds, the pieces and the reduce
+    qx, sx = wl.random_codes((M, K), 101), wl.random_scales((K // TILE, M), 102)
+    qw, sw = wl.random_codes((N, K), 103), wl.random_scales((N // TILE, K // TILE), 104)
+    dqx, dsx, dqw, dsw = to_dev(qx), scales_to_dev(sx), to_dev(qw), to_dev(sw)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    n, _ = _launches(lambda: bfp8.fp8_block_gemm_fwd(dqx, dsx, dqw, dsw, y, workspace=workspace))
+    assert n == 3
+    want = y.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        bfp8.fp8_block_gemm_fwd(dqx, dsx, dqw, dsw, y, workspace=workspace)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bfp8.fp8_block_gemm_fwd(dqx, dsx, dqw, dsw, y, workspace=workspace)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), want.view(torch.int16))
+    # doubled activation scales double every output exactly (a power of two)
+    dsx.mul_(2.0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.float(), 2.0 * want.float())
